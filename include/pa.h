@@ -1,0 +1,221 @@
+/*
+ * pa.h -- C ABI of libpa: paged GQA decode attention for GB300 (sm_103a).
+ *
+ * The library holds three things:
+ *   1. a fixed-block K/V page allocator (host metadata only),
+ *   2. an append kernel that scatters newly written K/V rows into their pages,
+ *   3. a split-K decode kernel that reads K/V through a block table, plus the
+ *      log-sum-exp merge of its splits.
+ *
+ * Conventions for every entry point:
+ *   - Pointers marked "device" are CUDA device pointers owned by the caller
+ *     (for example torch tensors); the library never frees them.  Pointers
+ *     marked "host" are ordinary host memory.
+ *   - Calls that take a stream are asynchronous and stream-ordered.  Errors
+ *     found on the host (bad sizes, unsupported shapes, null pointers) are
+ *     returned before anything is launched.  Errors found on the device (a
+ *     table entry outside the pool, a bounded wait that expired) are written
+ *     to the caller's device error word `err` (first error wins) and read back
+ *     with pa_get_error().
+ *   - No call allocates device memory.  Scratch space for pa_decode is passed
+ *     in by the caller, sized by pa_decode_workspace_size().
+ *
+ * Data layout (a reading of the pages; they describe a pool of pages plus a
+ * page table but print no byte layout):
+ *   K pool and V pool are separate device buffers, each
+ *       pool[block][kv_head][slot][row_bytes]
+ *   with slot in [0, page_size).  Row (seq s, position p) of kv head g lives
+ *   in block block_table[s * table_stride + p / page_size] at slot
+ *   p % page_size.  Each (block, kv_head) run of page_size rows is contiguous,
+ *   so a page is copied with one bulk transfer per head.
+ *   Row formats are ggml's: F16 (IEEE binary16, 2*head_dim bytes), Q8_0
+ *   (32-value blocks: fp16 scale d, 32 int8 q, value q*d; 34 bytes) and Q4_0
+ *   (32-value blocks: fp16 d, 16 bytes whose byte j holds element j in the low
+ *   nibble and element j+16 in the high nibble, value (nibble-8)*d; 18 bytes).
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; 0 is the legacy default stream. */
+typedef struct CUstream_st* pa_stream_t;
+
+typedef enum {
+  PA_OK = 0,
+  PA_ERR_INVALID = 1,     /* bad argument: null pointer, size, alignment, length */
+  PA_ERR_UNSUPPORTED = 2, /* shape or format this build does not implement */
+  PA_ERR_OOM = 3,         /* not enough free blocks; nothing was allocated */
+  PA_ERR_STALE = 4,       /* a handle is released, unknown or repeated; nothing was released */
+  PA_ERR_BOUNDS = 5,      /* device: a table entry or position outside the pool or table */
+  PA_ERR_TIMEOUT = 6,     /* device: a bounded wait inside a kernel expired */
+  PA_ERR_CUDA = 7         /* a CUDA runtime call failed */
+} pa_status;
+
+/* Row formats, numbered as ggml numbers them. */
+typedef enum { PA_F16 = 1, PA_Q4_0 = 2, PA_Q8_0 = 8 } pa_type;
+
+typedef struct {
+  uint32_t n_blocks;   /* blocks in the pool, 1 .. 2^31-1 */
+  uint32_t page_size;  /* positions (rows) per block, >= 1 */
+  uint32_t n_kv_heads; /* KV heads per row */
+  uint32_t head_dim;   /* values per row; multiple of 32 */
+  int32_t k_type;      /* pa_type of K rows */
+  int32_t v_type;      /* pa_type of V rows */
+} pa_pool_desc;
+
+/* A block handle: (generation << 32) | block index. */
+typedef uint64_t pa_block;
+
+typedef struct pa_pool pa_pool;
+
+/* ------------------------------------------------------------------ allocator
+ * "An exact fixed-block paged K/V allocator (transactional allocation,
+ * stale-handle detection, immediate release)" -- lucebox PR #555, Summary.
+ * Host metadata only; the K and V pools themselves are device buffers of
+ * pa_pool_bytes() bytes that the caller allocates.  Thread-safe (one mutex
+ * per pool). */
+
+/* Create a pool's allocator state.  PA_ERR_INVALID for a zero or oversize
+ * field, PA_ERR_UNSUPPORTED for an unknown type.  *out is owned by the
+ * caller and freed with pa_pool_destroy. */
+pa_status pa_pool_create(const pa_pool_desc* desc, pa_pool** out);
+
+/* Free the allocator state (not the device pools).  NULL is ignored. */
+void pa_pool_destroy(pa_pool* pool);
+
+/* Copy of the descriptor the pool was created with. */
+pa_status pa_pool_get_desc(const pa_pool* pool, pa_pool_desc* out);
+
+/* Bytes of one stored row of `head_dim` values of `type`; 0 if unsupported. */
+size_t pa_row_bytes(int32_t type, uint32_t head_dim);
+
+/* Bytes of the device K pool (which = 0) or V pool (which = 1):
+ * n_blocks * n_kv_heads * page_size * row_bytes.  0 for a bad argument. */
+size_t pa_pool_bytes(const pa_pool* pool, int which);
+
+/* Allocate n blocks, all or nothing.  Writes n handles to out (host).
+ * Blocks come from a LIFO free list that starts as 0, 1, 2, ...; a block
+ * released earlier is handed out again first.  PA_ERR_OOM (pool unchanged)
+ * when fewer than n blocks are free. */
+pa_status pa_alloc_blocks(pa_pool* pool, uint32_t n, pa_block* out);
+
+/* Release n handles (host array), all or nothing, immediately: the blocks
+ * are free on return and the handles become stale (the block's generation
+ * is bumped).  PA_ERR_STALE, with nothing released, if any handle is out of
+ * range, not allocated, of an old generation, or repeated in the call.  The
+ * caller must make sure no queued kernel still reads or writes the blocks. */
+pa_status pa_release(pa_pool* pool, const pa_block* handles, uint32_t n);
+
+/* Block index of a live handle, for building block tables.  PA_ERR_STALE
+ * for a handle that is not live. */
+pa_status pa_block_index(const pa_pool* pool, pa_block handle, int32_t* idx);
+
+/* Number of free blocks. */
+uint32_t pa_pool_free_count(const pa_pool* pool);
+
+/* ------------------------------------------------------------------ append
+ * Upload newly appended rows once, then scatter them into their page slots
+ * ("upload only newly appended KV rows through one packed transfer and
+ * scatter kernel" -- colibri PR #372, Summary; "writes map cells to pool rows
+ * through k/v idxs" -- llama.cpp fork PR #2, KV-pool commit).
+ *
+ * k_rows, v_rows: device, packed [n_rows][n_kv_heads][row_bytes], already in
+ *                 storage format; 16-byte aligned.
+ * row_seq, row_pos: device int32 [n_rows]: sequence and position of each row.
+ *                 Positions are appended in order with no gap (a row is
+ *                 written at the sequence's current length, lucebox PR #555,
+ *                 first-token bookkeeping fix); the kernel does not check it.
+ * block_table:    device int32 [n_seq][table_stride].
+ * k_pool, v_pool: device pools (pa_pool_bytes each), 16-byte aligned.
+ * err:            device int32 error word.
+ * A row whose sequence, page or table entry is out of range is skipped and
+ * sets *err = PA_ERR_BOUNDS; no out-of-range address is written.  The copy
+ * is byte-exact.  Rows with the same (seq, pos) in one call race. */
+pa_status pa_append_rows(const pa_pool* pool, void* k_pool, void* v_pool, const void* k_rows,
+                         const void* v_rows, const int32_t* row_seq, const int32_t* row_pos,
+                         uint32_t n_rows, const int32_t* block_table, uint32_t table_stride,
+                         uint32_t n_seq, int32_t* err, pa_stream_t stream);
+
+/* ------------------------------------------------------------------ decode
+ * Single-step GQA decode attention over a paged cache: split-K flash decoding
+ * through a block table, with a log-sum-exp merge of the splits ("Split-K
+ * flash decoding for head size 256, GQA 6 and 1-4 query tokens (MTP verify
+ * widths)", llama.cpp fork PR #2; "stable split-softmax merge", lucebox
+ * PR #555, Summary).
+ *
+ * For sequence s with L = seq_lens[s] cached rows (the n_qtok new rows
+ * included), query token t in [0, n_qtok) sits at position L - n_qtok + t and
+ * attends to keys 0 .. L - n_qtok + t.  Query head h reads KV head
+ * h / (n_q_heads / n_kv_heads).  Logits are scale * q.k; the output is the
+ * softmax-weighted sum of V rows, and lse the natural-log log-sum-exp of the
+ * scaled, masked logits ("max + log(rowsum)", llama.cpp fork PR #2, LSE
+ * commit).  A row with no visible key would give out = 0 and lse = -inf.
+ *
+ * Supported: head_dim 256, n_q_heads / n_kv_heads = 6, n_qtok 1..4, K and V
+ * each F16, Q4_0 or Q8_0 (PA_ERR_UNSUPPORTED otherwise).
+ *
+ * q:            device fp32 [n_seq][n_qtok][n_q_heads][head_dim], 16-byte aligned.
+ * k_pool/v_pool: device pools laid out as described at the top.
+ * block_table:  device int32 [n_seq][table_stride]; only entries for pages
+ *               holding positions < seq_lens[s] are read.
+ * seq_lens_dev / seq_lens_host: the same int32 [n_seq] lengths on the device
+ *               and on the host (the host copy sizes the launch).  Each
+ *               length must be >= n_qtok and <= table_stride * page_size
+ *               (PA_ERR_INVALID otherwise).
+ * out:          device fp32 [n_seq][n_qtok][n_q_heads][head_dim], 16-byte aligned.
+ * lse:          device fp32 [n_seq][n_qtok][n_q_heads], or NULL.
+ * workspace:    device scratch of ws_bytes >= pa_decode_workspace_size(),
+ *               256-byte aligned; its contents need no initialisation and
+ *               are garbage afterwards.  Concurrent calls need separate
+ *               workspaces.
+ * err:          device int32 error word.  A table entry outside [0, n_blocks)
+ *               sets *err = PA_ERR_BOUNDS; the rows it would have supplied are
+ *               read as zeros (no out-of-range read).
+ * The result depends only on the inputs and on seq_lens (not on page size or
+ * page placement): a paged cache and an identity-table cache holding the same
+ * rows give bit-identical outputs. */
+pa_status pa_decode(const pa_pool* pool, const float* q, const void* k_pool, const void* v_pool,
+                    const int32_t* block_table, uint32_t table_stride, const int32_t* seq_lens_dev,
+                    const int32_t* seq_lens_host, uint32_t n_seq, uint32_t n_qtok,
+                    uint32_t n_q_heads, float scale, float* out, float* lse, void* workspace,
+                    size_t ws_bytes, int32_t* err, pa_stream_t stream);
+
+/* Scratch bytes pa_decode needs for up to n_seq sequences of n_qtok query
+ * tokens on CUDA device `device`, whatever their lengths ("report the scratch
+ * up front so a tight budget fails at load", llama.cpp fork PR #2, scratch
+ * commit).  0 for an unsupported shape. */
+size_t pa_decode_workspace_size(const pa_pool* pool, uint32_t n_seq, uint32_t n_qtok, int device);
+
+/* How pa_decode would split this batch: *n_ctas decode CTAs, *n_tiles key
+ * tiles of `*tile_keys` keys each in total, and *n_partials split partials.
+ * Host only; for tests and tools. */
+pa_status pa_decode_plan(const pa_pool* pool, const int32_t* seq_lens_host, uint32_t n_seq,
+                         uint32_t n_qtok, int device, uint32_t* n_ctas, uint32_t* n_tiles,
+                         uint32_t* tile_keys, uint32_t* n_partials);
+
+/* ------------------------------------------------------------------ errors */
+
+/* Synchronise `stream`, read the device error word, reset it to 0 and return
+ * it as a pa_status (PA_ERR_CUDA if the read itself fails). */
+pa_status pa_get_error(int32_t* err, pa_stream_t stream);
+
+/* Static, human-readable name of a status. */
+const char* pa_status_string(pa_status s);
+
+/* Runs one kernel that waits, with the same bounded wait the decode kernel
+ * uses, on a shared-memory barrier that nothing ever completes; after about
+ * timeout_us microseconds the wait gives up and sets *err = PA_ERR_TIMEOUT.
+ * Exists so tests can check the expiry path without hanging a GPU. */
+pa_status pa_selftest_wait_timeout(uint32_t timeout_us, int32_t* err, pa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H */

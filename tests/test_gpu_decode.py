@@ -1,0 +1,229 @@
+"""Decode parity: the CUDA path against the float64 oracle, element by element,
+plus the bit-identity gates (paged == contiguous for any page size, repeats
+identical) and the controls that must fail (TensorFold #1156, Verification)."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from gpu_helpers import assert_close, assert_lse_close, device_cache, run_decode, to_dev
+from paged_kv_gqa_11_gb300 import (PA_ERR_BOUNDS, PA_ERR_TIMEOUT, PA_OK, _build, pa_decode_plan,
+                                   pa_selftest_wait_timeout)
+
+pytestmark = pytest.mark.gpu
+THREADS = os.cpu_count() or 1
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    _build.build()
+    oracle.build()
+
+
+F16, Q4, Q8 = W.TYPE_F16, W.TYPE_Q4_0, W.TYPE_Q8_0
+
+# (name, lengths, page size, K type, V type, n_qtok, layout): several tiles,
+# ragged tails, page sizes that do and do not divide the 64-key tile.
+SMALL = [
+    ("f16-1tok", [300], 16, F16, F16, 1, "shuffled"),
+    ("q4-edges", [1, 63, 64, 65, 129], 16, Q4, Q4, 1, "shuffled"),
+    ("q8-ps3-2tok", [200, 7], 3, Q8, Q8, 2, "shuffled"),
+    ("q8-masked-4tok", [513, 64, 4], 256, Q8, Q8, 4, "shuffled"),
+    ("f16-ps48-3tok", [1000, 130], 48, F16, F16, 3, "interleaved"),
+    ("q4-ps1-4tok", [777], 1, Q4, Q4, 4, "shuffled"),
+    ("q4-mix-2tok", [2048, 333, 17, 4096], 64, Q4, Q4, 2, "shuffled"),
+    ("q8-min-len", [1, 2, 3], 16, Q8, Q8, 1, "shuffled"),
+    ("f16-min-len-4tok", [4, 5, 6, 67], 16, F16, F16, 4, "shuffled"),
+]
+
+
+@pytest.mark.parametrize("name,lens,ps,kt,vt,nq,layout", SMALL, ids=[c[0] for c in SMALL])
+def test_small_parity(name, lens, ps, kt, vt, nq, layout):
+    w = W.make_workload(name, 200 + len(name), lens, ps, kt, vt, nq, layout)
+    go, gl = run_decode(w)
+    oo, ol = oracle.decode_workload(w, n_threads=THREADS)
+    assert_close(go, oo, what=name)
+    assert_lse_close(gl, ol, what=name)
+
+
+def test_many_short_sequences():
+    """More tiles than CTAs: CTAs walk many whole segments and restage Q."""
+    rng = np.random.default_rng(9)
+    lens = rng.integers(1, 300, size=200)
+    lens = np.maximum(lens, 2)
+    w = W.make_workload("many-short", 9, lens, 16, Q8, Q8, 2, "shuffled")
+    go, gl = run_decode(w)
+    oo, ol = oracle.decode_workload(w, n_threads=THREADS)
+    assert_close(go, oo, what="many-short")
+    assert_lse_close(gl, ol, what="many-short")
+
+
+def test_config1_tiny():
+    w = W.config(1)
+    go, gl = run_decode(w)
+    oo, ol = oracle.decode_workload(w)
+    assert_close(go, oo, what="config1")
+    assert_lse_close(gl, ol, what="config1")
+
+
+def test_config2_uniform():
+    w = W.config(2)
+    go, gl = run_decode(w)
+    oo, ol = oracle.decode_workload(w, n_threads=THREADS)
+    assert_close(go, oo, what="config2")
+    assert_lse_close(gl, ol, what="config2")
+
+
+def _sampled(w, pairs):
+    sel = np.zeros((w.n_seq, W.HQ), bool)
+    for s, h in pairs:
+        sel[s, h] = True
+    return sel
+
+
+@pytest.fixture(scope="module")
+def ragged():
+    w = W.config(3)
+    cache, tab = device_cache(w)
+    go, gl = run_decode(w, cache, tab)
+    return w, go, gl
+
+
+def test_config3_ragged_sampled(ragged):
+    w, go, gl = ragged
+    pairs = [(0, 0), (0, 7), (0, 23), (3, 12), (7, 5)]
+    oo, ol = oracle.decode_workload(w, n_threads=THREADS, select=_sampled(w, pairs))
+    for s, h in pairs:
+        assert_close(go[s, :, h], oo[s, :, h], what=f"config3 s{s} h{h}")
+        assert_lse_close(gl[s, :, h], ol[s, :, h], what=f"config3 s{s} h{h}")
+
+
+def test_config3_paged_equals_contiguous(ragged):
+    """Same rows through an identity table padded to 131072 slots per
+    sequence: bit-identical output (TensorFold #1156: paged == contiguous)."""
+    w, go, gl = ragged
+    wc = W.config(3, variant="contiguous")
+    co, cl = run_decode(wc)
+    assert np.array_equal(go, co) and np.array_equal(gl, cl)
+
+
+def test_page_size_invariance_and_repeats():
+    """Any page size and placement, same rows: bit-identical; three repeats
+    identical."""
+    base = W.make_workload("inv", 77, [3000, 129, 1025], 16, Q4, Q4, 3, "identity")
+    ref_o, ref_l = run_decode(base)
+    for ps in (1, 16, 48, 64, 256):
+        lists = W.interleaved_blocks(base.seq_lens, ps)
+        n = sum(len(l) for l in lists)
+        perm = np.random.default_rng(ps).permutation(n)
+        tab = W.table_from_lists([[int(perm[b]) for b in l] for l in lists])
+        w = W.Workload("inv", base.seq_lens, 3, ps, n, Q4, Q4, tab, base.k_rows, base.v_rows, base.q)
+        c, t = device_cache(w)
+        for _ in range(3):
+            o, l = run_decode(w, c, t)
+            assert np.array_equal(o, ref_o) and np.array_equal(l, ref_l), ps
+
+
+@pytest.mark.parametrize("nq", [1, 2, 3, 4])
+def test_config4_verify(nq):
+    w = W.config(4, n_qtok=nq)
+    go, gl = run_decode(w)
+    sel = _sampled(w, [(s, h) for s in range(4) for h in (0, 5, 6, 17, 23)])
+    oo, ol = oracle.decode_workload(w, n_threads=THREADS, select=sel)
+    for s in range(4):
+        for h in (0, 5, 6, 17, 23):
+            assert_close(go[s, :, h], oo[s, :, h], what=f"config4 nq{nq} s{s} h{h}")
+            assert_lse_close(gl[s, :, h], ol[s, :, h], what=f"config4 nq{nq} s{s} h{h}")
+
+
+def test_config5a_long_f16_sampled():
+    w = W.config(5, variant="a")
+    go, gl = run_decode(w)
+    pairs = [(0, 0), (0, 11), (0, 23)]
+    oo, ol = oracle.decode_workload(w, n_threads=THREADS, select=_sampled(w, pairs))
+    for s, h in pairs:
+        assert_close(go[s, :, h], oo[s, :, h], what=f"config5a h{h}")
+        assert_lse_close(gl[s, :, h], ol[s, :, h], what=f"config5a h{h}")
+
+
+def test_config5b_many_sampled():
+    w = W.config(5, variant="b")
+    go, gl = run_decode(w)
+    longest = int(np.argmax(w.seq_lens))
+    pairs = [(longest, 3), (0, 0), (17, 9), (40, 22), (63, 14)]
+    oo, ol = oracle.decode_workload(w, n_threads=THREADS, select=_sampled(w, pairs))
+    for s, h in pairs:
+        assert_close(go[s, :, h], oo[s, :, h], what=f"config5b s{s} h{h}")
+        assert_lse_close(gl[s, :, h], ol[s, :, h], what=f"config5b s{s} h{h}")
+
+
+def test_fully_masked_split_is_finite():
+    """L = 513 with 4 query tokens: the tile holding key 512 is visible only to
+    the last token; the merge must give finite output that matches."""
+    w = W.make_workload("mask", 88, [513], 256, Q8, Q8, 4, "shuffled")
+    go, gl = run_decode(w)
+    oo, ol = oracle.decode_workload(w)
+    assert np.isfinite(go).all() and np.isfinite(gl).all()
+    assert_close(go, oo, what="masked")
+
+
+def test_controls_are_red():
+    """A swapped table over correctly placed pages, and a planted row, must
+    both fail the comparison (TensorFold #1156: both controls red)."""
+    w = W.make_workload("ctl", 99, [700, 300], 16, Q4, Q4, 1, "shuffled")
+    oo, _ = oracle.decode_workload(w)
+    cache, tab = device_cache(w)
+    good, _ = run_decode(w, cache, tab)
+    assert_close(good, oo, what="control baseline")
+    # Attention is a function of the set of (k, v) rows, so the swap moves a
+    # page between sequences: sequence 0 then reads sequence 1's rows.
+    swapped = w.table.copy()
+    swapped[0, 2], swapped[1, 5] = w.table[1, 5], w.table[0, 2]
+    bad, _ = run_decode(w, cache, to_dev(swapped))
+    with pytest.raises(AssertionError):
+        assert_close(bad, oo, what="swapped table")
+    # planted row: overwrite K of position 100 (seq 1) with position 0's row
+    planted = w.k_rows.copy()
+    off = int(w.seq_offsets[1])
+    planted[off + 100] = planted[off + 0]
+    wp = W.Workload("ctl", w.seq_lens, 1, 16, w.n_blocks, Q4, Q4, w.table, planted, w.v_rows, w.q)
+    bad2, _ = run_decode(wp)
+    with pytest.raises(AssertionError):
+        assert_close(bad2, oo, what="planted row")
+
+
+def test_bounds_guard_reports_and_stays_finite():
+    w = W.make_workload("bnd", 5, [300, 80], 16, Q8, Q8, 1, "shuffled")
+    cache, tab = device_cache(w)
+    bad = w.table.copy()
+    bad[0, 3] = w.n_blocks + 1000
+    q = to_dev(w.q)
+    out, lse = cache.decode(q, to_dev(bad), to_dev(w.seq_lens), w.seq_lens, 1, w.scale)
+    torch.cuda.synchronize()
+    assert cache.check() == PA_ERR_BOUNDS
+    assert torch.isfinite(out).all()
+    # sequence 1 does not touch the bad entry: still exact
+    oo, _ = oracle.decode_workload(w)
+    assert_close(out.cpu().numpy()[1], oo[1], what="unaffected sequence")
+
+
+def test_bounded_wait_expires_with_status():
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    assert pa_selftest_wait_timeout(2000, err) == PA_OK
+    torch.cuda.synchronize()
+    assert int(err.item()) == PA_ERR_TIMEOUT
+
+
+def test_plan_covers_every_tile():
+    w = W.config(3)
+    from paged_kv_gqa_11_gb300.cache import PagedKVCache
+    c = PagedKVCache(w.n_blocks, w.page_size, w.k_type, w.v_type)
+    plan = pa_decode_plan(c.pool, w.seq_lens, 1)
+    tiles = int(sum((L + 63) // 64 for L in w.seq_lens)) * W.HKV
+    assert plan["tiles"] == tiles and plan["tile_keys"] == 64
+    assert 0 < plan["ctas"] <= tiles
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert plan["ctas"] % sms == 0 or plan["ctas"] == tiles
