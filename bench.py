@@ -1,0 +1,518 @@
+#!/usr/bin/env python
+"""Benchmark of paged GQA decode attention on GB300.
+
+Workload (default): the ragged 8-request decode of lucebox PR #555 ("Ragged
+8-request workload (128K + 7 x 8K, Q4_0 K/V)"): sequence lengths 131072 and
+7 x 8192 (188,416 live tokens), 16-token pages handed out round-robin as if the
+requests arrived together, Q4_0 K/V from N(0,1) sources, D=256, 24 query heads
+on 4 KV heads, one query token.  Synthetic, seeded inputs.
+
+One step = one pa_decode (split-K pass + merge pass) over the whole batch.
+Metric: K/V GB/s = algorithmic K+V bytes read per step (every live row of
+every KV head once) / step time, and us/step.  L2 is flushed (a 2 x L2 write)
+between timed steps, outside the timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Multi-GPU (torchrun): every rank decodes its own copy of the batch, with no
+data-path communication (the (sequence, KV head) segments are independent);
+the value is the bytes all ranks processed over the slowest rank's time.
+--impl reference times the float64 CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "paged decode attention K/V GB/s (fraction of GB300 HBM peak) and us/step"
+FALLBACK_HBM_GBS = 6800.0
+# RTX 3090, paged, same workload: 4.095 ms per step (lucebox PR #555, ragged
+# table) = 217,055,232 B / 4.095 ms = 53.0 GB/s.  Another machine: context.
+PAGES_PAGED_3090_MS = 4.095
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_split_ragged_q4_0.md")
+DECODE_SOURCES = ["paged_kv_gqa_11_gb300/csrc/pa_decode.cu", "paged_kv_gqa_11_gb300/csrc/pa_decode_impl.cuh",
+                  "paged_kv_gqa_11_gb300/csrc/pa_decode_kern_q4_0.cu", "paged_kv_gqa_11_gb300/csrc/pa_device.cuh"]
+
+
+def workload_for(name: str) -> W.Workload:
+    if name == "ragged":
+        return W.config(3)
+    if name == "ragged-contiguous":
+        return W.config(3, variant="contiguous")
+    if name == "uniform":
+        return W.config(2)
+    if name.startswith("verify"):
+        return W.config(4, n_qtok=int(name[-1]) if name[-1].isdigit() else 4)
+    if name == "long":
+        return W.config(5, variant="a")
+    if name == "many":
+        return W.config(5, variant="b")
+    raise SystemExit(f"unknown workload {name}")
+
+
+def describe(w: W.Workload) -> str:
+    lens = w.seq_lens
+    if len(set(lens.tolist())) == 1:
+        shape = f"{len(lens)}x{int(lens[0])}"
+    elif len(lens) <= 8:
+        shape = "+".join(str(int(x)) for x in lens)
+    else:
+        shape = f"{len(lens)} seqs, sum {int(lens.sum())}, max {int(lens.max())}"
+    kt = W.TYPE_NAMES[w.k_type]
+    vt = W.TYPE_NAMES[w.v_type]
+    return (f"{w.name}: paged GQA decode, lengths {shape}, page size {w.page_size}, K {kt} / V {vt}, "
+            f"D=256, Hq=24, Hkv=4, {w.n_qtok} query token(s)")
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in DECODE_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profile_traffic(workload: str):
+    """DRAM bytes per launch of the split kernel from the committed ncu summary,
+    if it was taken on this workload with the current kernel source."""
+    try:
+        text = open(PROFILE_SUMMARY).read()
+    except OSError:
+        return None
+    vals = {}
+    for line in text.splitlines():
+        if line.startswith("traffic:"):
+            for kv in line[len("traffic:"):].split(";"):
+                if "=" in kv:
+                    k, v = kv.split("=", 1)
+                    vals[k.strip()] = v.strip()
+    if vals.get("source") != source_hash() or vals.get("workload") != workload:
+        return None
+    try:
+        return int(vals["bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except OSError:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 20):
+        self.gpu = gpu_index
+        self.period = period_ms
+        self.proc = None
+        self.lines = []
+        self.t_begin = self.t_end = None
+
+    def begin(self):
+        """Mark the start of the timed region (samples before it are ignored)."""
+        from datetime import datetime
+        self.t_begin = datetime.now()
+
+    def end(self):
+        from datetime import datetime
+        self.t_end = datetime.now()
+        time.sleep(3 * self.period / 1000.0)
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 f"-lms", str(self.period)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+            time.sleep(0.3)  # let the first samples arrive
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        from datetime import datetime
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                ts = datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
+            except ValueError:
+                continue
+            if self.t_begin and ts < self.t_begin or self.t_end and ts > self.t_end:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _select(w: W.Workload, pairs):
+    sel = np.zeros((w.n_seq, W.HQ), bool)
+    for s, g in pairs:
+        sel[s, g * W.GQA:(g + 1) * W.GQA] = True
+    return sel
+
+
+def oracle_segments(w: W.Workload, cache, budget_s: float, threads: int):
+    """A bounded sample of the workload for the float64 oracle: whole
+    (sequence, KV head) segments, shortest first, added until one run of the
+    sample is estimated to take about budget_s on `threads` host threads."""
+    import oracle
+    segs = sorted((int(w.seq_lens[s]), s, g) for s in range(w.n_seq) for g in range(W.HKV))
+    L0, s0, g0 = segs[0]
+    t0 = time.perf_counter()
+    oracle.decode(cache, w.q, w.scale, _select(w, [(s0, g0)]), n_threads=threads)
+    per_row = max(time.perf_counter() - t0, 1e-5) / L0
+    chosen, est = [], 0.0
+    for L, s, g in segs:
+        if chosen and est + L * per_row > budget_s:
+            break
+        chosen.append((s, g))
+        est += L * per_row
+    return chosen
+
+
+def oracle_time(w: W.Workload, cache, pairs, threads: int) -> float:
+    import oracle
+    t0 = time.perf_counter()
+    oracle.decode(cache, w.q, w.scale, _select(w, pairs), n_threads=threads)
+    return time.perf_counter() - t0
+
+
+def sample_bytes(w: W.Workload, pairs) -> int:
+    rb = W.row_bytes(w.k_type) + W.row_bytes(w.v_type)
+    return sum(int(w.seq_lens[s]) for s, _ in pairs) * rb
+
+
+def sample_desc(w: W.Workload, pairs) -> str:
+    rows = sum(int(w.seq_lens[s]) for s, _ in pairs)
+    return (f"{len(pairs)} of {w.n_seq * W.HKV} (sequence, KV head) segments, shortest first, "
+            f"{rows} K/V rows, all {W.GQA * w.n_qtok} query rows of each")
+
+
+def oracle_cache(w: W.Workload):
+    import oracle
+    oracle.build()
+    return oracle.Cache.from_workload(w)
+
+
+def run_reference(args, w: W.Workload):
+    """The float64 oracle on the host cores, each step a bounded sample."""
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    threads = os.cpu_count() or 1
+    cache = oracle_cache(w)
+    per_step = max(0.05, 120.0 / max(1, args.steps + args.warmup))
+    pairs = oracle_segments(w, cache, per_step, threads)
+    times = []
+    for i in range(args.warmup + args.steps):
+        dt = oracle_time(w, cache, pairs, threads)
+        if i >= args.warmup:
+            times.append(dt)
+    step = statistics.mean(times)
+    value = sample_bytes(w, pairs) / step / 1e9
+    desc = sample_desc(w, pairs)
+    line = {
+        "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(step * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": describe(w), "sample": desc, "l2": "n/a (CPU)"},
+        "impl": "reference",
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="ragged")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+
+    w = workload_for(args.workload)
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import paged_kv_gqa_11_gb300 as pa
+    from paged_kv_gqa_11_gb300.cache import PagedKVCache
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    cache = PagedKVCache(w.n_blocks, w.page_size, w.k_type, w.v_type, device=dev)
+    table = t(w.table)
+    cache.append(t(w.k_rows), t(w.v_rows), t(w.row_seq), t(w.row_pos), table)
+    sl_dev = t(w.seq_lens)
+    sl_host = np.ascontiguousarray(w.seq_lens, np.int32)
+    ws = cache.workspace(w.n_seq, w.n_qtok)
+    if cache.check() != pa.PA_OK:
+        raise SystemExit("append reported a device error")
+    kv_bytes = w.kv_bytes()
+    plan = pa.pa_decode_plan(cache.pool, sl_host, w.n_qtok, local)
+
+    # Step inputs (query + one new K/V row per sequence + its index) packed in
+    # one buffer, outputs (out + lse) in another: one H2D and one D2H per step
+    # in the end-to-end leg.
+    new_idx = np.array([int(w.seq_offsets[s + 1]) - 1 for s in range(w.n_seq)])  # last row of each sequence
+    parts_in = [np.ascontiguousarray(w.q).view(np.uint8).ravel(),
+                np.ascontiguousarray(w.k_rows[new_idx]).view(np.uint8).ravel(),
+                np.ascontiguousarray(w.v_rows[new_idx]).view(np.uint8).ravel(),
+                np.ascontiguousarray(w.row_seq[new_idx]).view(np.uint8).ravel(),
+                np.ascontiguousarray(w.row_pos[new_idx]).view(np.uint8).ravel()]
+    offs, o = [], 0
+    for a in parts_in:
+        offs.append(o)
+        o += (a.nbytes + 255) // 256 * 256
+    h_in = torch.zeros(o, dtype=torch.uint8).pin_memory()
+    for a, off in zip(parts_in, offs):
+        h_in[off:off + a.nbytes] = torch.from_numpy(a)
+    d_in = h_in.to(dev)
+    view = lambda buf, i, dtype, shape: buf[offs[i]:offs[i] + parts_in[i].nbytes].view(dtype).view(shape)
+    q = view(d_in, 0, torch.float32, w.q.shape)
+    d_k = view(d_in, 1, torch.uint8, (w.n_seq,) + w.k_rows.shape[1:])
+    d_v = view(d_in, 2, torch.uint8, (w.n_seq,) + w.v_rows.shape[1:])
+    d_seq = view(d_in, 3, torch.int32, (w.n_seq,))
+    d_pos = view(d_in, 4, torch.int32, (w.n_seq,))
+    n_out = w.n_seq * w.n_qtok * W.HQ * W.D
+    d_outbuf = torch.empty(n_out + w.n_seq * w.n_qtok * W.HQ, dtype=torch.float32, device=dev)
+    h_outbuf = torch.empty(d_outbuf.shape, dtype=torch.float32).pin_memory()
+    out = d_outbuf[:n_out].view(w.n_seq, w.n_qtok, W.HQ, W.D)
+    lse = d_outbuf[n_out:].view(w.n_seq, w.n_qtok, W.HQ)
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_buf = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def decode(passes):
+        pa.pa_decode(cache.pool, q, cache.k_pool, cache.v_pool, table, table.shape[1], sl_dev, sl_host, w.n_seq,
+                     w.n_qtok, W.HQ, w.scale, out, lse, ws, ws.numel(), cache.err, stream.cuda_stream,
+                     passes=passes)
+
+    for _ in range(args.warmup):
+        flush_buf.fill_(1.0)
+        decode("all")
+    torch.cuda.synchronize()
+    if cache.check() != pa.PA_OK:
+        raise SystemExit("decode reported a device error")
+
+    # ---- timed steps: one pa_decode (split + merge) each, L2 flushed between
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    with ClockSampler(local) as clocks:
+        barrier()
+        torch.cuda.synchronize()
+        clocks.begin()
+        wall0 = time.perf_counter()
+        for i in range(K):
+            flush_buf.fill_(1.0)
+            ev[i][0].record(stream)
+            decode("all")
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        wall = time.perf_counter() - wall0
+        clocks.end()
+    my_step = statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in range(K))
+    if cache.check() != pa.PA_OK:
+        raise SystemExit("decode reported a device error")
+
+    # ---- the split kernel alone (the roofline's kernel): split pass timed, merge after it
+    KS = max(3, min(K, 1000))
+    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(KS)]
+    barrier()
+    torch.cuda.synchronize()
+    for i in range(KS):
+        flush_buf.fill_(1.0)
+        sev[i][0].record(stream)
+        decode("split")
+        sev[i][1].record(stream)
+        decode("merge")
+    torch.cuda.synchronize()
+    barrier()
+    my_split = statistics.mean(sev[i][0].elapsed_time(sev[i][1]) for i in range(KS))
+
+    # ---- end to end through the public API: packed host inputs in, host outputs back
+    h2d = h_in.numel()
+    d2h = h_outbuf.numel() * 4
+
+    def e2e_step():
+        d_in.copy_(h_in, non_blocking=True)
+        cache.append(d_k, d_v, d_seq, d_pos, table, stream=stream.cuda_stream)
+        decode("all")
+        h_outbuf.copy_(d_outbuf, non_blocking=True)
+
+    for _ in range(3):
+        flush_buf.fill_(1.0)
+        e2e_step()
+    torch.cuda.synchronize()
+    E = args.e2e_steps
+    eev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(E)]
+    barrier()
+    torch.cuda.synchronize()
+    for i in range(E):
+        flush_buf.fill_(1.0)
+        eev[i][0].record(stream)
+        e2e_step()
+        eev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    my_e2e = statistics.mean(eev[i][0].elapsed_time(eev[i][1]) for i in range(E))
+    if cache.check() != pa.PA_OK:
+        raise SystemExit("end-to-end step reported a device error")
+    if not np.isfinite(h_outbuf.numpy()).all():
+        raise SystemExit("non-finite output")
+
+    # ---- max over ranks
+    def rank_max(x):
+        if dist is None:
+            return x
+        tt = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        return float(tt.item())
+
+    step = rank_max(my_step)
+    split = rank_max(my_split)
+    e2e = rank_max(my_e2e)
+    n = world
+    value = n * kv_bytes / (step * 1e-3) / 1e9
+    achieved = kv_bytes / (split * 1e-3) / 1e9
+    peaks = measured_peaks()
+    peak = float(peaks["hbm_gbs"]) if peaks and "hbm_gbs" in peaks else FALLBACK_HBM_GBS
+    peak_src = "measured (MEASURED_PEAKS.json hbm_gbs, copy)" if peaks else "fallback"
+
+    cpu = None
+    if rank == 0 and n == 1 and not args.no_cpu_baseline:
+        threads = os.cpu_count() or 1
+        ocache = oracle_cache(w)
+        pairs = oracle_segments(w, ocache, args.cpu_budget, threads)
+        secs = oracle_time(w, ocache, pairs, threads)
+        cpu = {"value": round(sample_bytes(w, pairs) / secs / 1e9, 4), "unit": "GB/s", "cores": threads,
+               "kind": "oracle", "sample": sample_desc(w, pairs) + f"; {secs:.1f} s wall on {threads} threads"}
+
+    if dist is not None:
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+    wl = args.workload
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": n,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(step, 5),
+        "us_per_step": round(step * 1e3, 2),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": round(value / (kv_bytes / (PAGES_PAGED_3090_MS * 1e-3) / 1e9), 2) if wl == "ragged" else None,
+        "vs_baseline_note": "vs RTX 3090 paged 4.095 ms/step on the same workload (lucebox PR #555); context only"
+        if wl == "ragged" else None,
+        "dtype": "f16",
+        "data": "synthetic",
+        "config": {
+            "workload": describe(w),
+            "kv_bytes_per_step": kv_bytes,
+            "kv_storage": f"K {W.TYPE_NAMES[w.k_type]} / V {W.TYPE_NAMES[w.v_type]}",
+            "arithmetic": "fp16 tensor-core products, fp32 accumulation and softmax",
+            "l2": "flushed (2 x L2 write) between timed steps, outside the timed region",
+            "plan": plan,
+            "timing": "CUDA events on the launching stream around each pa_decode (split + merge), mean over steps",
+            "wall_s": round(wall, 3),
+        },
+        "frac_of_hbm_peak": round(value / n / peak, 4),
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "pa_split_decode_kernel",
+            "achieved": round(achieved, 2),
+            "peak": peak,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": profile_traffic(wl),
+            "peak_source": peak_src,
+            "split_us": round(split * 1e3, 2),
+        },
+        "e2e": {"value": round(n * kv_bytes / (e2e * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "us_per_step": round(e2e * 1e3, 2), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 2 * K,  # split + merge kernels per timed step
+        "clocks": clocks.summary(),
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

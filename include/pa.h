@@ -186,6 +186,24 @@ pa_status pa_decode(const pa_pool* pool, const float* q, const void* k_pool, con
                     uint32_t n_q_heads, float scale, float* out, float* lse, void* workspace,
                     size_t ws_bytes, int32_t* err, pa_stream_t stream);
 
+/* The two passes of pa_decode as separate calls, with pa_decode's arguments.
+ * pa_decode_split runs the split-K pass: sequences handled by one CTA get
+ * their final out/lse, the others leave split partials in `workspace`.
+ * pa_decode_merge then merges those partials into out/lse.  Calling split then
+ * merge on one stream, with the same arguments and workspace and nothing in
+ * between that touches the workspace, is exactly pa_decode; the split lets a
+ * caller time or schedule the passes separately. */
+pa_status pa_decode_split(const pa_pool* pool, const float* q, const void* k_pool, const void* v_pool,
+                          const int32_t* block_table, uint32_t table_stride, const int32_t* seq_lens_dev,
+                          const int32_t* seq_lens_host, uint32_t n_seq, uint32_t n_qtok, uint32_t n_q_heads,
+                          float scale, float* out, float* lse, void* workspace, size_t ws_bytes, int32_t* err,
+                          pa_stream_t stream);
+pa_status pa_decode_merge(const pa_pool* pool, const float* q, const void* k_pool, const void* v_pool,
+                          const int32_t* block_table, uint32_t table_stride, const int32_t* seq_lens_dev,
+                          const int32_t* seq_lens_host, uint32_t n_seq, uint32_t n_qtok, uint32_t n_q_heads,
+                          float scale, float* out, float* lse, void* workspace, size_t ws_bytes, int32_t* err,
+                          pa_stream_t stream);
+
 /* Scratch bytes pa_decode needs for up to n_seq sequences of n_qtok query
  * tokens on CUDA device `device`, whatever their lengths ("report the scratch
  * up front so a tight budget fails at load", llama.cpp fork PR #2, scratch

@@ -31,7 +31,7 @@ PA_OK, PA_ERR_INVALID, PA_ERR_UNSUPPORTED, PA_ERR_OOM, PA_ERR_STALE, PA_ERR_BOUN
 # Every entry point declared in include/pa.h.
 EXPORTS = ["pa_pool_create", "pa_pool_destroy", "pa_pool_get_desc", "pa_row_bytes", "pa_pool_bytes",
            "pa_alloc_blocks", "pa_release", "pa_block_index", "pa_pool_free_count", "pa_append_rows",
-           "pa_decode", "pa_decode_workspace_size", "pa_decode_plan", "pa_get_error", "pa_status_string",
+           "pa_decode", "pa_decode_split", "pa_decode_merge", "pa_decode_workspace_size", "pa_decode_plan", "pa_get_error", "pa_status_string",
            "pa_selftest_wait_timeout"]
 
 
@@ -89,6 +89,7 @@ def load():
             "pa_status_string": (C.c_char_p, [C.c_int]),
             "pa_selftest_wait_timeout": (C.c_int, [u32, vp, vp]),
         }
+        sig["pa_decode_split"] = sig["pa_decode_merge"] = sig["pa_decode"]
         for name, (res, args) in sig.items():
             f = getattr(L, name)
             f.restype = res
@@ -204,10 +205,12 @@ def pa_decode_plan(pool: Pool, seq_lens_host, n_qtok: int, device: int = 0) -> d
 
 def pa_decode(pool: Pool, q, k_pool, v_pool, block_table, table_stride: int, seq_lens_dev, seq_lens_host,
               n_seq: int, n_qtok: int, n_q_heads: int, scale: float, out, lse, workspace, ws_bytes: int, err,
-              stream=None, check: bool = True) -> int:
+              stream=None, check: bool = True, passes: str = "all") -> int:
     """seq_lens_host: a host int32 buffer (numpy array or address) that stays
-    alive for the call."""
-    rc = load().pa_decode(pool.handle, _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table), table_stride,
+    alive for the call.  passes: "all" (pa_decode), "split" (pa_decode_split)
+    or "merge" (pa_decode_merge)."""
+    fn = {"all": "pa_decode", "split": "pa_decode_split", "merge": "pa_decode_merge"}[passes]
+    rc = getattr(load(), fn)(pool.handle, _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table), table_stride,
                           _ptr(seq_lens_dev), _ptr(seq_lens_host), n_seq, n_qtok, n_q_heads, C.c_float(scale),
                           _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes, _ptr(err), _stream(stream))
     if check:

@@ -17,7 +17,8 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libpa.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["pa_pool.cpp", "pa_append.cu", "pa_decode.cu"]
+SOURCES = ["pa_pool.cpp", "pa_append.cu", "pa_decode.cu", "pa_decode_kern_f16.cu", "pa_decode_kern_q4_0.cu",
+           "pa_decode_kern_q8_0.cu"]
 
 
 def _cuda_home() -> str:

@@ -53,7 +53,7 @@ class PagedKVCache:
 
     def decode(self, q: torch.Tensor, block_table: torch.Tensor, seq_lens_dev: torch.Tensor,
                seq_lens_host: np.ndarray, n_qtok: int, scale: float = 1.0 / 16.0, out: torch.Tensor | None = None,
-               lse: torch.Tensor | None = None, want_lse: bool = True, stream=None):
+               lse: torch.Tensor | None = None, want_lse: bool = True, stream=None, passes: str = "all"):
         """q: device fp32 [n_seq][n_qtok][n_q_heads][head_dim]; returns (out, lse)."""
         n_seq, _, hq, d = q.shape
         if out is None:
@@ -63,7 +63,7 @@ class PagedKVCache:
         sl = np.ascontiguousarray(seq_lens_host, dtype=np.int32)
         ws = self.workspace(n_seq, n_qtok)
         pa_decode(self.pool, q, self.k_pool, self.v_pool, block_table, int(block_table.shape[1]), seq_lens_dev, sl,
-                  n_seq, n_qtok, hq, scale, out, lse, ws, ws.numel(), self.err, stream)
+                  n_seq, n_qtok, hq, scale, out, lse, ws, ws.numel(), self.err, stream, passes=passes)
         return out, lse
 
     def check(self, stream=None) -> int:
