@@ -11,45 +11,47 @@
 // (mma.sync m16n8k16, fp16 operands, fp32 accumulation), the softmax is
 // online, and the splits are merged by log-sum-exp.
 //
-// Work split.  Every (sequence, KV head) is a segment of 64-key tiles.  All
-// tiles of the batch are laid end to end and cut into equal contiguous ranges,
-// one per CTA, with as many CTAs as fit on the SMs at once.  A CTA's range may
-// cover the tail of one segment and the head of the next; each piece becomes
-// one split partial.  The cut depends only on the sequence lengths, so a paged
-// and an identity-table cache give the same splits, the same summation order
-// and bit-identical results (TensorFold #1156, Design/Kernels: "only the
-// address changes; the per-key summation order does not").
+// Work split.  The batch is cut into segments (below), each a run of tiles.
+// All tiles are laid end to end and cut into equal contiguous ranges, one per
+// CTA, with as many CTAs as fit on the SMs at once.  A CTA's range may cover
+// the tail of one segment and the head of the next; each piece becomes one
+// split partial.  The cut depends only on the sequence lengths, so a paged and
+// an identity-table cache give the same splits, the same summation order and
+// bit-identical results (TensorFold #1156, Design/Kernels: "only the address
+// changes; the per-key summation order does not").
 //
 // Data movement.  One producer warp streams K and V tiles into a ring of
-// shared-memory stages with cp.async.bulk, one copy per page run (per row for
-// F16, into a padded layout that keeps fragment loads bank-conflict free),
-// completing on mbarriers.  The table is read once per page run and one tile
-// ahead (TensorFold #1156: "test once per block").  A table entry outside the
-// pool is never dereferenced: its rows are zero-filled, PA_ERR_BOUNDS recorded.
+// shared-memory stages with cp.async.bulk, completing on mbarriers.  The table
+// is read one tile ahead, once per page (TensorFold #1156: "test once per
+// block").  A table entry outside the pool is never dereferenced: its rows are
+// zero-filled and PA_ERR_BOUNDS is recorded.
 //
-// Compute, one query token (6 query rows).  Each of the four consumer warps
-// owns 16 keys of every tile end to end: S^T = K Q^T (M = keys, N = query
-// rows, K = dims), softmax, then O^T += V^T P^T over all 256 dims (M = dims,
-// N = rows, K = keys).  Warps never wait for each other inside a piece; their
-// four (max, sum, O) states are combined once per piece in shared memory.
-// The running max is raised only when a logit exceeds it by more than 2^8
-// (P <= 256 stays exact enough in fp16), so most tiles rescale nothing.
+// One query token ("head-group" tiles).  A segment is (sequence, group of up
+// to four KV heads); a tile is 16 keys of every head of the group, which for
+// 16-row pages is one whole pool block (all heads), copied in one transfer per
+// K and V.  Consumer warp w owns KV head w of the group end to end: it stages
+// its six query rows, computes S^T = K Q^T (M = keys, N = query rows,
+// K = dims), the softmax, and O^T += V^T P^T over all 256 dims (M = dims,
+// N = rows, K = keys).  Warps never wait for each other.  The running max is
+// raised only when a logit exceeds it by more than 2^8 (P <= 256 stays exact
+// enough in fp16), so most tiles rescale nothing.
 //
-// Compute, 2-4 query tokens (12-24 rows).  Holding O for all dims per warp
-// would take 64 registers per 8 rows, so the warps split the tile instead: in
-// the S phase warp w computes keys 16w..16w+15, publishes its tile max, row
+// Two to four query tokens ("per-head" tiles, 12-24 rows).  Holding O for all
+// dims per warp would take 64 registers per 8 rows, so the warps split the
+// tile instead: a segment is (sequence, KV head), a tile 64 keys of that head;
+// in the S phase warp w computes keys 16w..16w+15, publishes its tile max, row
 // sums and P (transposed with movmatrix) in shared memory, and after a named
 // barrier computes O^T for dims 64w..64w+63 over all 64 keys.
 //
 // Dequantisation.  K goes into the MMA as raw magic-biased halves: a Q4_0
 // nibble n becomes 1024+n (low) or 1024+16n (high nibble, against Q/16), a
 // Q8_0 byte x becomes 1152+x.  Each 32-dim block gets its own accumulator;
-// the bias (sum of the block's Q times 1032/1152, computed once per piece) is
-// subtracted and the block scale d applied in fp32.  V for one query token is
-// converted to the exact integers n-8 / x in fp16 and the block scale is folded
-// into P (each MMA's 16 dims lie in one block).  The head dims are visited in
-// whatever order makes each thread's loads contiguous; Q and the output use
-// the same order, so the dot products are unchanged.
+// the bias (sum of the block's Q times 1032/1152, computed with the staged Q)
+// is subtracted and the block scale d applied in fp32.  V for one query token
+// is converted to the exact integers n-8 / x in fp16 and the block scale is
+// folded into P (each MMA's 16 dims lie in one block).  The head dims are
+// visited in whatever order makes each thread's loads contiguous; Q and the
+// output use the same order, so the dot products are unchanged.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -65,10 +67,11 @@ namespace pa_split {
 
 using namespace pa_dev;
 
-constexpr int kD = 256;     // head dim
-constexpr int kGqa = 6;     // query heads per KV head
-constexpr int kTile = 64;   // keys per tile
-constexpr int kCWarps = 4;  // consumer warps
+constexpr int kD = 256;       // head dim
+constexpr int kGqa = 6;       // query heads per KV head
+constexpr int kTile = 64;     // keys per per-head tile (two or more query tokens)
+constexpr int kTileHG = 16;   // keys per head-group tile (one query token)
+constexpr int kCWarps = 4;    // consumer warps = heads per head group (at most)
 constexpr int kThreads = (kCWarps + 1) * 32;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -96,24 +99,34 @@ struct Fmt<PA_Q8_0> {
 
 // Shared memory outside the stage ring.
 constexpr int extras_bytes(int NT) {
-  return 2 * 16 * NT * 32 * 8         // Q fragments, double buffered
-         + 2 * 8 * NT * 8 * 4         // per-block bias corrections
-         + (NT == 1 ? (8 * 260 * 4 + kCWarps * 8 * 8)           // combine buffer + warp stats
-                    : (2 * kCWarps * NT * 32 * 8 + 2 * kCWarps * NT * 8 * 8))  // P + stats
+  return (NT == 1 ? kCWarps * (16 * 32 * 8 + 8 * 8 * 4)  // per-warp Q fragments + block corrections
+                  : (2 * 16 * NT * 32 * 8                  // Q fragments, double buffered
+                     + 2 * 8 * NT * 8 * 4                  // block corrections
+                     + 2 * kCWarps * NT * 32 * 8           // P fragments
+                     + 2 * kCWarps * NT * 8 * 8))          // tile stats
          + 2 * 8 * 8 + 32;  // barriers (up to 8 stages), misc
 }
+
+// Keys and heads one stage holds: 16 keys x 4 heads (one token) or 64 keys x
+// 1 head (more tokens).  Same bytes either way.
+template <int NT>
+struct TileShape {
+  static constexpr int kKeys = NT == 1 ? kTileHG : kTile;
+  static constexpr int kHeads = NT == 1 ? kCWarps : 1;
+  static constexpr int kRows = kKeys * kHeads;  // stored rows per stage for K (and for V)
+};
 
 // CTAs per SM a configuration aims for: three for one-token Q4_0 (small
 // stages, modest registers), otherwise two, or one when a stage is large.
 template <int KT, int VT, int NT>
 struct CtaTarget {
-  static constexpr int kStageBytes = kTile * (Fmt<KT>::kStride + Fmt<VT>::kStride);
+  static constexpr int kStageBytes = TileShape<NT>::kRows * (Fmt<KT>::kStride + Fmt<VT>::kStride);
   static constexpr int kN = (kStageBytes <= 20000 && NT == 1) ? 3 : (kStageBytes <= 40000 ? 2 : 1);
 };
 
 template <int KT, int VT, int NT>
 struct Stages {
-  static constexpr int kStageBytes = kTile * (Fmt<KT>::kStride + Fmt<VT>::kStride);
+  static constexpr int kStageBytes = TileShape<NT>::kRows * (Fmt<KT>::kStride + Fmt<VT>::kStride);
   static constexpr int kCtas = CtaTarget<KT, VT, NT>::kN;
   static constexpr int kBudget = (233472 - kCtas * 1024) / kCtas;  // 228 KB per SM, 1 KB reserved per CTA
   static constexpr int kPerCtaMax = kBudget < 232448 ? kBudget : 232448;
@@ -218,8 +231,12 @@ struct DecodeParams {
   float* out;
   float* lse;
   int32_t* err;
-  float2* part_ml;  // [slots][R] (m in log2 units, l)
-  float* part_o;    // [slots][R][kD]
+  float2* part_ml;  // [slots][rows_per_seg] (m in log2 units, l)
+  float* part_o;    // [slots][rows_per_seg][kD]
+  float2* mid_ml;   // [slots][rows_per_seg] merge level-1 results, indexed by a chunk's first slot
+  float* mid_o;     // [slots][rows_per_seg][kD]
+  int* merge_count; // [n_seg][rows_per_seg] level-1 arrivals; zeroed by the split kernel
+  int n_counters;   // n_seg * rows_per_seg
   long long total_tiles;
   int n_ctas;
   int n_seq;
@@ -229,6 +246,10 @@ struct DecodeParams {
   int page_size;
   int table_stride;
   int n_blocks;
+  int tile_keys;     // keys per tile: 16 (head groups) or 64 (single heads)
+  int seg_heads;     // KV heads per segment: the head-group size, or 1
+  int segs_per_seq;  // n_kv_heads / seg_heads
+  int rows_per_seg;  // query rows per segment: 6 * seg_heads * n_qtok
   float scale_log2;  // scale * log2(e)
 };
 
@@ -236,22 +257,25 @@ struct DecodeParams {
 template <int KT, int VT, int NT>
 struct Smem {
   static constexpr int kStages = Stages<KT, VT, NT>::kN;
-  static constexpr int kKBytes = kTile * Fmt<KT>::kStride;
-  static constexpr int kStageBytes = kTile * (Fmt<KT>::kStride + Fmt<VT>::kStride);
-  static constexpr int kQBuf = 16 * NT * 32 * 8;               // one Q fragment buffer
-  static constexpr int kQ = kStages * kStageBytes;             // [2][16][NT][32] uint2
-  static constexpr int kCbBuf = 8 * NT * 8 * 4;                // one correction buffer
-  static constexpr int kCb = kQ + 2 * kQBuf;                   // [2][8 blocks][NT*8 rows] float
-  static constexpr int kWork = kCb + 2 * kCbBuf;               // path-specific area
-  // one-token path: combine buffer [8][260] float, warp stats [4][8] float2
-  static constexpr int kComb = kWork;
-  static constexpr int kWStat = kComb + 8 * 260 * 4;
-  // multi-token path: P fragments [2][4][NT][32] uint2, stats [2][4][NT*8] float2
-  static constexpr int kP = kWork;
+  static constexpr int kKBytes = TileShape<NT>::kRows * Fmt<KT>::kStride;
+  static constexpr int kStageBytes = TileShape<NT>::kRows * (Fmt<KT>::kStride + Fmt<VT>::kStride);
+  static constexpr int kRing = kStages * kStageBytes;
+  // head-group path: per-warp Q fragments [4][16][32] uint2, corrections [4][8][8] float
+  static constexpr int kWQ = kRing;
+  static constexpr int kWQBytes = 16 * 32 * 8;
+  static constexpr int kWCb = kWQ + kCWarps * kWQBytes;
+  static constexpr int kWCbBytes = 8 * 8 * 4;
+  // per-head path: Q fragments [2][16][NT][32] uint2, corrections [2][8][NT*8],
+  // P fragments [2][4][NT][32] uint2, stats [2][4][NT*8] float2
+  static constexpr int kQBuf = 16 * NT * 32 * 8;
+  static constexpr int kQ = kRing;
+  static constexpr int kCbBuf = 8 * NT * 8 * 4;
+  static constexpr int kCb = kQ + 2 * kQBuf;
+  static constexpr int kP = kCb + 2 * kCbBuf;
   static constexpr int kStat = kP + 2 * kCWarps * NT * 32 * 8;
-  static constexpr int kWorkEnd = NT == 1 ? kWStat + kCWarps * 8 * 8 : kStat + 2 * kCWarps * NT * 8 * 8;
-  static constexpr int kBar = kWorkEnd;                        // full[kStages], empty[kStages]
-  static constexpr int kMisc = kBar + 2 * kStages * 8;         // abort flag, start position
+  static constexpr int kWorkEnd = NT == 1 ? kWCb + kCWarps * kWCbBytes : kStat + 2 * kCWarps * NT * 8 * 8;
+  static constexpr int kBar = kWorkEnd;                 // full[kStages], empty[kStages]
+  static constexpr int kMisc = kBar + 2 * kStages * 8;  // abort flag, start position
   static constexpr int kTotal = kMisc + 32;
 };
 
@@ -259,12 +283,15 @@ __device__ __forceinline__ int cta_of_tile(long long x, long long T, int G) {
   return (int)(((x + 1) * (long long)G - 1) / T);
 }
 
-// Find the segment holding global tile x: sequence s, KV head g, tile j within it.
+__device__ __forceinline__ int tiles_of(const DecodeParams& p, int L) { return (L + p.tile_keys - 1) / p.tile_keys; }
+
+// Find the segment holding global tile x: sequence s, segment-in-sequence g
+// (KV head, or head group), tile j within it.
 __device__ __forceinline__ void locate_tile(const DecodeParams& p, long long x, int& s_out, int& g_out, int& j_out) {
   long long base = 0;
   for (int s = 0; s < p.n_seq; ++s) {
-    const long long nt = (p.seq_lens[s] + kTile - 1) / kTile;
-    const long long span = nt * p.n_kv_heads;
+    const long long nt = tiles_of(p, p.seq_lens[s]);
+    const long long span = nt * p.segs_per_seq;
     if (x < base + span) {
       const long long r = x - base;
       s_out = s;
@@ -280,7 +307,7 @@ __device__ __forceinline__ void locate_tile(const DecodeParams& p, long long x, 
 }
 
 // Position of one tile in the CTA's walk: sequence s (length L, nt tiles),
-// KV head g, tile j of that (sequence, head) segment.
+// segment g of that sequence, tile j of the segment.
 struct TilePos {
   int s, g, j, L, nt;
 };
@@ -288,17 +315,17 @@ struct TilePos {
 __device__ __forceinline__ void next_tile(const DecodeParams& p, TilePos& t) {
   if (++t.j < t.nt) return;
   t.j = 0;
-  if (++t.g < p.n_kv_heads) return;
+  if (++t.g < p.segs_per_seq) return;
   t.g = 0;
   if (++t.s < p.n_seq) {
     t.L = p.seq_lens[t.s];
-    t.nt = (t.L + kTile - 1) / kTile;
+    t.nt = tiles_of(p, t.L);
   }
 }
 
-// Table entries one lane needs for a tile: per-row copies use rows lane and
-// lane+32, per-page copies pages p0+lane and p0+lane+32 (a 64-row tile spans
-// at most 64 pages).  -1 where the lane has nothing.
+// Table entries one lane needs for a per-head tile: per-row copies use rows
+// lane and lane+32, per-page copies pages p0+lane and p0+lane+32 (a 64-row
+// tile spans at most 64 pages).  -1 where the lane has nothing.
 template <bool kPerRow>
 __device__ __forceinline__ void load_tile_table(const DecodeParams& p, const TilePos& t, int lane, int (&tb)[2]) {
   const int32_t* trow = p.table + (long long)t.s * p.table_stride;
@@ -317,14 +344,141 @@ __device__ __forceinline__ void load_tile_table(const DecodeParams& p, const Til
   }
 }
 
+// Table entry for a head-group tile (16 keys, so at most 16 pages): lane l
+// holds page p0 + l.
+__device__ __forceinline__ int load_hg_table(const DecodeParams& p, const TilePos& t, int lane) {
+  const int32_t* trow = p.table + (long long)t.s * p.table_stride;
+  const int k0 = t.j * kTileHG, n = min(kTileHG, t.L - k0), ps = p.page_size;
+  const int p0 = k0 / ps, p1 = (k0 + n - 1) / ps;
+  return (p0 + lane <= p1) ? __ldg(trow + p0 + lane) : -1;
+}
+
+// Producer for head-group tiles: stage = K [4 heads][16 rows][SK] then V.
+// A full 16-row page whose group covers every KV head is one contiguous pool
+// block per K and V: one copy each.  Otherwise one copy per (page, head) run,
+// or per row for the padded F16 layout.
+template <int KT, int VT, int NT>
+__device__ void produce_hg(const DecodeParams& p, uint8_t* smem, uint32_t bar_full, uint32_t bar_empty,
+                           volatile int* abort, long long a, long long b, TilePos pos) {
+  constexpr int kStages = Stages<KT, VT, NT>::kN;
+  constexpr int RK = Fmt<KT>::kRow, RV = Fmt<VT>::kRow;
+  constexpr int SK = Fmt<KT>::kStride, SV = Fmt<VT>::kStride;
+  constexpr bool kPerRow = (SK != RK) || (SV != RV);
+  constexpr int kStageBytes = TileShape<NT>::kRows * (SK + SV);
+  constexpr int kHeadK = kTileHG * SK, kHeadV = kTileHG * SV;  // one head's rows in a stage
+  const int lane = threadIdx.x & 31;
+  const uint32_t stage0 = smem_u32(smem);
+  const int ps = p.page_size, H = p.n_kv_heads, GH = p.seg_heads;
+  const bool whole_blocks = (ps == kTileHG) && (GH == H);
+  const uint64_t policy = l2_evict_first_policy();
+  int st = 0;
+  uint32_t ph = 0;
+  long long issued = 0;
+  int tb = load_hg_table(p, pos, lane), tbn = -1;
+  for (long long x = a; x < b; ++x) {
+    if (*abort) break;
+    TilePos nxt = pos;
+    if (x + 1 < b) {
+      next_tile(p, nxt);
+      tbn = load_hg_table(p, nxt, lane);
+    }
+    const uint32_t fb = bar_full + 8 * st, eb = bar_empty + 8 * st;
+    const int k0 = pos.j * kTileHG;
+    const int n = min(kTileHG, pos.L - k0);
+    const int p0 = k0 / ps, p1 = (k0 + n - 1) / ps;
+    const bool used = p0 + lane <= p1;
+    const bool ok = !used || (tb >= 0 && tb < p.n_blocks);
+    const bool all_ok = __all_sync(0xffffffffu, ok);
+    const bool fast = all_ok && n == kTileHG && whole_blocks && !kPerRow;
+    if (lane == 0) mbar_wait(eb, ph ^ 1, p.err, abort);
+    __syncwarp();
+    const uint32_t sk = stage0 + st * kStageBytes, sv = sk + kCWarps * kHeadK;
+    const int h0 = pos.g * GH;  // first KV head of the group
+    if (fast) {
+      if (lane == 0) {
+        mbar_arrive_expect_tx(fb, (uint32_t)H * kTileHG * (RK + RV));
+        const long long row = (long long)tb * H * ps;  // block base, head 0, slot 0
+        bulk_g2s_hint(sk, p.k_pool + row * RK, (uint32_t)H * kTileHG * RK, fb, policy);
+        bulk_g2s_hint(sv, p.v_pool + row * RV, (uint32_t)H * kTileHG * RV, fb, policy);
+      }
+      __syncwarp();
+    } else {
+      if (!ok) record_error(p.err, PA_ERR_BOUNDS);
+      // Lane covers row r = lane & 15 of heads (lane >> 4) and (lane >> 4) + 2.
+      // Every lane takes part in the shuffle.
+      const int r = lane & 15;
+      const int pg_r = (k0 + r) / ps;
+      const int blk_r = __shfl_sync(0xffffffffu, tb, min(pg_r - p0, 31));
+      const bool row_ok = r < n && blk_r >= 0 && blk_r < p.n_blocks;
+      uint32_t bytes = 0;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int w = (lane >> 4) + 2 * k;
+        if (w < GH && row_ok) {
+          if (kPerRow) bytes += RK + RV;
+        } else {
+          for (int c = 0; c < RK; c += 16) sts128_zero(sk + w * kHeadK + r * SK + c);
+          for (int c = 0; c < RV; c += 16) sts128_zero(sv + w * kHeadV + r * SV + c);
+        }
+      }
+      // Page runs (packed layouts): the page's lane counts the run for all heads.
+      int rs = 0, re = 0;
+      if (!kPerRow && used && ok) {
+        rs = max(k0, (p0 + lane) * ps);
+        re = min(k0 + n, (p0 + lane + 1) * ps);
+        bytes += (uint32_t)(re - rs) * GH * (RK + RV);
+      }
+      fence_proxy_async_smem();
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
+      __syncwarp();
+      if (lane == 0) mbar_arrive_expect_tx(fb, bytes);
+      __syncwarp();
+      if (kPerRow) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int w = (lane >> 4) + 2 * k;
+          if (w < GH && row_ok) {
+            const long long row = ((long long)blk_r * H + h0 + w) * ps + (k0 + r) % ps;
+            bulk_g2s_hint(sk + w * kHeadK + r * SK, p.k_pool + row * RK, RK, fb, policy);
+            bulk_g2s_hint(sv + w * kHeadV + r * SV, p.v_pool + row * RV, RV, fb, policy);
+          }
+        }
+      } else if (used && ok) {
+        const int pg = p0 + lane;
+        for (int w = 0; w < GH; ++w) {
+          const long long row = ((long long)tb * H + h0 + w) * ps + (rs - pg * ps);
+          bulk_g2s_hint(sk + w * kHeadK + (rs - k0) * SK, p.k_pool + row * RK, (re - rs) * RK, fb, policy);
+          bulk_g2s_hint(sv + w * kHeadV + (rs - k0) * SV, p.v_pool + row * RV, (re - rs) * RV, fb, policy);
+        }
+      }
+    }
+    ++issued;
+    if (++st == kStages) { st = 0; ph ^= 1; }
+    pos = nxt;
+    tb = tbn;
+  }
+  // Drain: make sure no copy is still in flight when the CTA retires.
+  if (lane == 0) {
+    const int n_last = (int)(issued < kStages ? issued : kStages);
+    for (int k = 1; k <= n_last; ++k) {
+      int sst = st - k;
+      uint32_t sph = ph;
+      if (sst < 0) { sst += kStages; sph ^= 1; }
+      mbar_wait(bar_full + 8 * sst, sph, p.err, abort, /*honour_abort=*/false);
+    }
+  }
+}
+
 // ------------------------------------------------------------------ producer
 
-// Producer warp: stream the CTA's tiles into the stage ring.  The table
+// Producer for per-head tiles (64 keys of one KV head): stream the CTA's
+// tiles into the stage ring.  The table
 // entries of tile i+1 are loaded while tile i is waited for and issued, so the
 // table's latency stays off the refill path.  A full tile whose entries are
 // all valid takes the fast path (no zero fill, byte count known).
 template <int KT, int VT, int NT>
-__device__ void produce(const DecodeParams& p, uint8_t* smem, uint32_t bar_full, uint32_t bar_empty,
+__device__ void produce_head(const DecodeParams& p, uint8_t* smem, uint32_t bar_full, uint32_t bar_empty,
                         volatile int* abort, long long a, long long b, TilePos pos) {
   constexpr int kStages = Stages<KT, VT, NT>::kN;
   constexpr int RK = Fmt<KT>::kRow, RV = Fmt<VT>::kRow;
@@ -440,6 +594,76 @@ __device__ void produce(const DecodeParams& p, uint8_t* smem, uint32_t bar_full,
       mbar_wait(bar_full + 8 * sst, sph, p.err, abort, /*honour_abort=*/false);
     }
   }
+}
+
+// Head-group path: warp w stages its own KV head's six query rows (one
+// query token) as S-MMA B fragments ([k-step][lane] uint2) and the per-block
+// bias corrections cb[block][row], from coalesced float4 loads.  Rows 6 and 7
+// of the fragment (padding) are zero.  Only this warp reads them.
+template <int KT>
+__device__ __forceinline__ int kdim_inverse(int d, int& ks, int& jj) {
+  // returns nothing useful; fills the k-step and k-index that hold dim d
+  int t, u, h, e;
+  if (KT == PA_F16) {
+    const int c = d >> 6, r = d & 63;
+    t = r >> 4; u = (r & 15) >> 2; h = (r >> 1) & 1; e = r & 1;
+    ks = 4 * c + u;
+  } else if (KT == PA_Q8_0) {
+    const int b = d >> 5, r = d & 31;
+    t = r >> 3; u = (r >> 2) & 1; h = r & 1; e = (r >> 1) & 1;
+    ks = 2 * b + u;
+  } else {  // Q4_0
+    const int b = d >> 5, r = d & 31;
+    u = r >> 4; t = (r & 15) >> 2; h = r & 1; e = (r >> 1) & 1;
+    ks = 2 * b + u;
+  }
+  jj = 2 * t + 8 * h + e;
+  return t;
+}
+
+template <int KT>
+__device__ void stage_q_warp(const DecodeParams& p, int s, int head, uint32_t qf, float* cb, int lane) {
+  // zero the padding rows 6, 7 (lanes 24..31 of every k-step) and their
+  // corrections, so the padding logits are exactly 0
+  if (lane >= 24) {
+#pragma unroll
+    for (int ks = 0; ks < 16; ++ks)
+      asm volatile("st.shared.v2.b32 [%0], {%1, %1};" ::"r"(qf + (ks * 32 + lane) * 8), "r"(0u) : "memory");
+  }
+  if (KT != PA_F16 && lane < 16) cb[(lane >> 1) * 8 + 6 + (lane & 1)] = 0.f;
+  const float4* q4 = reinterpret_cast<const float4*>(p.q + ((long long)s * p.n_q_heads + head * kGqa) * kD);
+#pragma unroll 4
+  for (int i = 0; i < kGqa * kD / 4 / 32; ++i) {  // 12 float4 per lane
+    const int f = lane + 32 * i;
+    const int row = f >> 6, d0 = 4 * (f & 63);
+    const float4 v = __ldg(q4 + f);
+    const float vals[4] = {v.x, v.y, v.z, v.w};
+    float lo = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int d = d0 + k;
+      int ks, jj;
+      const int t = kdim_inverse<KT>(d, ks, jj);
+      const float sc = (KT == PA_Q4_0 && (ks & 1)) ? 0.0625f : 1.f;
+      const __half hv = __float2half_rn(sc * vals[k]);
+      lo += __half2float(hv);
+      const int ln = 4 * row + t;
+      const uint32_t addr = qf + (ks * 32 + ln) * 8 + ((jj >> 3) << 2) + ((jj & 1) << 1);
+      asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(__half_as_ushort(hv)) : "memory");
+    }
+    if (KT != PA_F16) {
+      // lanes 8b'..8b'+7 hold the 8 float4 of block 4(i&1)+b' of row i/2:
+      // k < 4 low 16 dims, k >= 4 high 16 dims.
+      lo += __shfl_xor_sync(0xffffffffu, lo, 1);
+      lo += __shfl_xor_sync(0xffffffffu, lo, 2);
+      const float hi = __shfl_down_sync(0xffffffffu, lo, 4);
+      if ((lane & 7) == 0) {
+        const int blk = 4 * (i & 1) + (lane >> 3);
+        cb[blk * 8 + (i >> 1)] = (KT == PA_Q4_0) ? 1032.f * lo + 1152.f * hi : 1152.f * (lo + hi);
+      }
+    }
+  }
+  __syncwarp();
 }
 
 // ------------------------------------------------------------------ Q staging
@@ -754,39 +978,34 @@ __device__ __forceinline__ void write_row_stats(const DecodeParams& p, bool whol
   }
 }
 
-// ------------------------------------------------------------------ consumers
+// ------------------------------------------------------------------ head-group consumer
 
-// One-token path (NT = 1): see the file comment.
+// One query token: warp w owns KV head (group * GH + w); see the file comment.
 template <int KT, int VT>
-__device__ void consume_solo(const DecodeParams& p, uint8_t* smem, uint32_t bar_full, uint32_t bar_empty,
-                             volatile int* abort, long long a, long long b, int s, int g, int j) {
+__device__ void consume_hg(const DecodeParams& p, uint8_t* smem, uint32_t bar_full, uint32_t bar_empty,
+                           volatile int* abort, long long a, long long b, int s, int g, int j) {
   using SM = Smem<KT, VT, 1>;
   constexpr int kStages = SM::kStages;
   constexpr int SK = Fmt<KT>::kStride, SV = Fmt<VT>::kStride;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gq = lane >> 2, tq = lane & 3;
-  const int R = kGqa;  // one query token
   const uint32_t sbase = smem_u32(smem);
-  float* comb = reinterpret_cast<float*>(smem + SM::kComb);
-  float2* wstat = reinterpret_cast<float2*>(smem + SM::kWStat);
-  const long long T = p.total_tiles;
-  const int G = p.n_ctas;
+  const uint32_t qf = sbase + SM::kWQ + warp * SM::kWQBytes;
+  float* cb = reinterpret_cast<float*>(smem + SM::kWCb + warp * SM::kWCbBytes);
+  const uint32_t qf_lane = qf + lane * 8;
+  const uint32_t cb_lane = smem_u32(cb) + 2 * tq * 4;
+  const bool active = warp < p.seg_heads;
   int st = 0;
   uint32_t ph = 0;
-  int qbuf = 0;
   long long x = a;
   while (x < b) {
     const int L = p.seq_lens[s];
-    const int ntl = (L + kTile - 1) / kTile;
+    const int ntl = tiles_of(p, L);
     const int jb = j, je = (int)((long long)ntl < j + (b - x) ? (long long)ntl : j + (b - x));
-    const int seg = s * p.n_kv_heads + g;
+    const int seg = s * p.segs_per_seq + g;
     const bool whole = (jb == 0 && je == ntl);
-    const uint32_t qf = sbase + SM::kQ + qbuf * SM::kQBuf;
-    float* cb = reinterpret_cast<float*>(smem + SM::kCb + qbuf * SM::kCbBuf);
-    stage_q<KT, 1>(p, s, g, qf, cb, tid);
-    named_bar_sync(1, kCWarps * 32);
-    const uint32_t qf_lane = qf + lane * 8;
-    const uint32_t cb_lane = smem_u32(cb) + 2 * tq * 4;
+    const int head = g * p.seg_heads + warp;
+    if (active) stage_q_warp<KT>(p, s, head, qf, cb, lane);
 
     float o[16][4];
 #pragma unroll
@@ -796,66 +1015,56 @@ __device__ void consume_solo(const DecodeParams& p, uint8_t* smem, uint32_t bar_
     float mref0 = -INFINITY, mref1 = -INFINITY;  // rows 2tq, 2tq+1
     float ls0 = 0.f, ls1 = 0.f;                  // this thread's share of the row sums
 
-    const int vis0 = L - p.n_qtok;  // last key visible to query token 0
+    const int vis = L - 1;  // last visible key (one query token)
     for (int jt = jb; jt < je; ++jt) {
       if (!*abort) mbar_wait(bar_full + 8 * st, ph, p.err, abort);
-      const uint32_t sk = sbase + st * SM::kStageBytes;
-      const uint32_t sv = sk + SM::kKBytes;
-      const int k0 = jt * kTile;
-      // ---- S for keys 16*warp + gq and + 8
-      float sacc[1][4] = {{0.f, 0.f, 0.f, 0.f}};
-      {
-        const uint32_t r0 = sk + (16 * warp + gq) * SK;
-        s_phase<KT, 1>(sacc, r0, r0 + 8 * SK, qf_lane, cb_lane, lane);
-      }
-      float xv[4];
-      const int key0 = k0 + 16 * warp + gq;
-      const bool need_mask = (k0 + kTile - 1) > vis0;
+      if (active) {
+        const uint32_t sk = sbase + st * SM::kStageBytes + warp * (kTileHG * SK);
+        const uint32_t sv = sbase + st * SM::kStageBytes + SM::kKBytes + warp * (kTileHG * SV);
+        const int k0 = jt * kTileHG;
+        float sacc[1][4] = {{0.f, 0.f, 0.f, 0.f}};
+        s_phase<KT, 1>(sacc, sk + gq * SK, sk + (gq + 8) * SK, qf_lane, cb_lane, lane);
+        float xv[4];
+        const bool need_mask = (k0 + kTileHG - 1) > vis;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        xv[c] = sacc[0][c] * p.scale_log2;
-        if (need_mask) {
-          const int row = 2 * tq + (c & 1);
-          const int tk = min(row / kGqa, p.n_qtok - 1);
-          if (key0 + ((c & 2) ? 8 : 0) > vis0 + tk) xv[c] = -INFINITY;
+        for (int c = 0; c < 4; ++c) {
+          xv[c] = sacc[0][c] * p.scale_log2;
+          if (need_mask && k0 + gq + ((c & 2) ? 8 : 0) > vis) xv[c] = -INFINITY;
         }
-      }
-      // ---- lazy running max
-      const bool up = (xv[0] > mref0 + kLazy) || (xv[2] > mref0 + kLazy) || (xv[1] > mref1 + kLazy) ||
-                      (xv[3] > mref1 + kLazy);
-      if (__any_sync(0xffffffffu, up)) {
-        float mx0 = fmaxf(xv[0], xv[2]), mx1 = fmaxf(xv[1], xv[3]);
+        // ---- lazy running max
+        const bool up = (xv[0] > mref0 + kLazy) || (xv[2] > mref0 + kLazy) || (xv[1] > mref1 + kLazy) ||
+                        (xv[3] > mref1 + kLazy);
+        if (__any_sync(0xffffffffu, up)) {
+          float mx0 = fmaxf(xv[0], xv[2]), mx1 = fmaxf(xv[1], xv[3]);
 #pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-        }
-        const float mn0 = fmaxf(mref0, mx0), mn1 = fmaxf(mref1, mx1);
-        const float al0 = (mn0 == -INFINITY) ? 1.f : exp2f(mref0 - mn0);
-        const float al1 = (mn1 == -INFINITY) ? 1.f : exp2f(mref1 - mn1);
+          for (int off = 4; off < 32; off <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+          }
+          const float mn0 = fmaxf(mref0, mx0), mn1 = fmaxf(mref1, mx1);
+          const float al0 = (mn0 == -INFINITY) ? 1.f : exp2f(mref0 - mn0);
+          const float al1 = (mn1 == -INFINITY) ? 1.f : exp2f(mref1 - mn1);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          o[i][0] *= al0; o[i][2] *= al0;
-          o[i][1] *= al1; o[i][3] *= al1;
+          for (int i = 0; i < 16; ++i) {
+            o[i][0] *= al0; o[i][2] *= al0;
+            o[i][1] *= al1; o[i][3] *= al1;
+          }
+          ls0 *= al0;
+          ls1 *= al1;
+          mref0 = mn0;
+          mref1 = mn1;
         }
-        ls0 *= al0;
-        ls1 *= al1;
-        mref0 = mn0;
-        mref1 = mn1;
-      }
-      const float b0 = (mref0 == -INFINITY) ? 0.f : mref0, b1 = (mref1 == -INFINITY) ? 0.f : mref1;
-      const uint32_t X0 = pack_half2(exp2f(xv[0] - b0), exp2f(xv[1] - b1));  // key gq: rows 2tq, 2tq+1
-      const uint32_t X1 = pack_half2(exp2f(xv[2] - b0), exp2f(xv[3] - b1));  // key gq+8
-      {
-        const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&X0));
-        const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&X1));
-        ls0 += f0.x + f1.x;
-        ls1 += f0.y + f1.y;
-      }
-      const uint32_t B0 = movmatrix_trans(X0), B1 = movmatrix_trans(X1);
-      // ---- O^T += V^T P^T over this warp's 16 keys
-      {
-        const uint32_t v0 = sv + (16 * warp + 2 * tq) * SV;
+        const float b0 = (mref0 == -INFINITY) ? 0.f : mref0, b1 = (mref1 == -INFINITY) ? 0.f : mref1;
+        const uint32_t X0 = pack_half2(exp2f(xv[0] - b0), exp2f(xv[1] - b1));  // key gq: rows 2tq, 2tq+1
+        const uint32_t X1 = pack_half2(exp2f(xv[2] - b0), exp2f(xv[3] - b1));  // key gq+8
+        {
+          const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&X0));
+          const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&X1));
+          ls0 += f0.x + f1.x;
+          ls1 += f0.y + f1.y;
+        }
+        const uint32_t B0 = movmatrix_trans(X0), B1 = movmatrix_trans(X1);
+        const uint32_t v0 = sv + 2 * tq * SV;
         const uint32_t rows[4] = {v0, v0 + SV, v0 + 8 * SV, v0 + 9 * SV};
         pv_solo<VT>(o, rows, lane, B0, B1);
       }
@@ -864,73 +1073,50 @@ __device__ void consume_solo(const DecodeParams& p, uint8_t* smem, uint32_t bar_
       if (++st == kStages) { st = 0; ph ^= 1; }
     }
 
-    // ---- combine the four warps' states for this piece
+    // ---- piece result for this warp's head: rows 2tq, 2tq+1 (< 6)
+    if (active) {
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      ls0 += __shfl_xor_sync(0xffffffffu, ls0, off);
-      ls1 += __shfl_xor_sync(0xffffffffu, ls1, off);
-    }
-    if (gq == 0) {
-      wstat[warp * 8 + 2 * tq] = make_float2(mref0, ls0);
-      wstat[warp * 8 + 2 * tq + 1] = make_float2(mref1, ls1);
-    }
-    named_bar_sync(1, kCWarps * 32);
-    float fsel[2];
+      for (int off = 4; off < 32; off <<= 1) {
+        ls0 += __shfl_xor_sync(0xffffffffu, ls0, off);
+        ls1 += __shfl_xor_sync(0xffffffffu, ls1, off);
+      }
+      const int slot = (int)blockIdx.x + seg;
 #pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      const int row = 2 * tq + c;
-      float M = -INFINITY;
+      for (int c = 0; c < 2; ++c) {
+        const int hl = 2 * tq + c;
+        if (hl >= kGqa) continue;
+        const float lr = c ? ls1 : ls0, mr = c ? mref1 : mref0;
+        const int row = warp * kGqa + hl;  // row within the segment
+        float* dst;
+        float inv = 1.f;
+        if (whole) {
+          dst = p.out + ((long long)s * p.n_q_heads + head * kGqa + hl) * kD;
+          inv = lr > 0.f ? 1.f / lr : 0.f;
+        } else {
+          dst = p.part_o + ((long long)slot * p.rows_per_seg + row) * kD;
+        }
 #pragma unroll
-      for (int w2 = 0; w2 < kCWarps; ++w2) M = fmaxf(M, wstat[w2 * 8 + row].x);
-      const float mine = wstat[warp * 8 + row].x;
-      fsel[c] = (M == -INFINITY || mine == -INFINITY) ? 0.f : exp2f(mine - M);
-    }
-    // Deterministic order: warp 0 writes, warps 1..3 add in turn.
-    for (int w2 = 0; w2 < kCWarps; ++w2) {
-      if (warp == w2) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int row = 2 * tq + (c & 1);
-            if (row < R) {
-              float* dst = comb + row * 260 + vdim_solo<VT>(gq, i, c >> 1);
-              const float v = fsel[c & 1] * o[i][c];
-              *dst = (w2 == 0) ? v : *dst + v;
-            }
+        for (int i = 0; i < 16; ++i) {
+          dst[vdim_solo<VT>(gq, i, 0)] = o[i][c] * inv;
+          dst[vdim_solo<VT>(gq, i, 1)] = o[i][2 + c] * inv;
+        }
+        if (gq == 0) {
+          if (whole) {
+            if (p.lse) p.lse[(long long)s * p.n_q_heads + head * kGqa + hl] = lr > 0.f ? (mr + log2f(lr)) * kLn2 : -INFINITY;
+          } else {
+            p.part_ml[(long long)slot * p.rows_per_seg + row] = make_float2(mr, lr);
           }
+        }
       }
-      named_bar_sync(1, kCWarps * 32);
-    }
-    // Rows 0..R-1, 256 dims: coalesced output by all consumer threads.
-    const int slot = (int)blockIdx.x + seg;
-    for (int e = tid; e < R * (kD / 4); e += kCWarps * 32) {
-      const int row = e / (kD / 4), d4 = e % (kD / 4);
-      float M = -INFINITY, Lsum = 0.f;
-#pragma unroll
-      for (int w2 = 0; w2 < kCWarps; ++w2) M = fmaxf(M, wstat[w2 * 8 + row].x);
-#pragma unroll
-      for (int w2 = 0; w2 < kCWarps; ++w2) {
-        const float2 v = wstat[w2 * 8 + row];
-        if (v.x != -INFINITY) Lsum += exp2f(v.x - M) * v.y;
-      }
-      float4 val = *reinterpret_cast<const float4*>(comb + row * 260 + 4 * d4);
-      if (whole) {
-        const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-        val.x *= inv; val.y *= inv; val.z *= inv; val.w *= inv;
-      }
-      reinterpret_cast<float4*>(row_dst(p, whole, slot, s, g, row, R))[d4] = val;
-      if (d4 == 0) write_row_stats(p, whole, slot, s, g, row, R, M, Lsum);
     }
 
     x += je - jb;
-    qbuf ^= 1;
     j = 0;
-    if (++g == p.n_kv_heads) { g = 0; ++s; }
+    if (++g == p.segs_per_seq) { g = 0; ++s; }
   }
-  (void)T;
-  (void)G;
 }
+
+// ------------------------------------------------------------------ per-head consumer
 
 // Multi-token path (NT = 2, 3): see the file comment.
 template <int KT, int VT, int NT>
@@ -951,9 +1137,9 @@ __device__ void consume_shared(const DecodeParams& p, uint8_t* smem, uint32_t ba
   long long x = a;
   while (x < b) {
     const int L = p.seq_lens[s];
-    const int ntl = (L + kTile - 1) / kTile;
+    const int ntl = tiles_of(p, L);
     const int jb = j, je = (int)((long long)ntl < j + (b - x) ? (long long)ntl : j + (b - x));
-    const int seg = s * p.n_kv_heads + g;
+    const int seg = s * p.segs_per_seq + g;
     const bool whole = (jb == 0 && je == ntl);
     const uint32_t qf = sbase + SM::kQ + qbuf * SM::kQBuf;
     float* cb = reinterpret_cast<float*>(smem + SM::kCb + qbuf * SM::kCbBuf);
@@ -1114,7 +1300,7 @@ __device__ void consume_shared(const DecodeParams& p, uint8_t* smem, uint32_t ba
     x += je - jb;
     qbuf ^= 1;
     j = 0;
-    if (++g == p.n_kv_heads) { g = 0; ++s; }
+    if (++g == p.segs_per_seq) { g = 0; ++s; }
   }
 }
 
@@ -1136,6 +1322,9 @@ __global__ void __launch_bounds__(kThreads, CtaTarget<KT, VT, NT>::kN)
   const int G = p.n_ctas;
   const long long a = (long long)blockIdx.x * T / G, b = (long long)(blockIdx.x + 1) * T / G;
 
+  // Zero the merge kernel's arrival counters (it reads them only after the
+  // whole split grid has finished).
+  for (int i = blockIdx.x * kThreads + tid; i < p.n_counters; i += gridDim.x * kThreads) p.merge_count[i] = 0;
   if (tid == 0) {
     // The merge kernel may launch now; it reads nothing of ours before its
     // griddepcontrol.wait.
@@ -1161,12 +1350,16 @@ __global__ void __launch_bounds__(kThreads, CtaTarget<KT, VT, NT>::kN)
     pos.g = g;
     pos.j = j;
     pos.L = p.seq_lens[s];
-    pos.nt = (pos.L + kTile - 1) / kTile;
-    produce<KT, VT, NT>(p, smem, bar_full, bar_empty, abort, a, b, pos);
+    pos.nt = tiles_of(p, pos.L);
+    if constexpr (NT == 1) {
+      produce_hg<KT, VT, NT>(p, smem, bar_full, bar_empty, abort, a, b, pos);
+    } else {
+      produce_head<KT, VT, NT>(p, smem, bar_full, bar_empty, abort, a, b, pos);
+    }
     return;
   }
   if constexpr (NT == 1) {
-    consume_solo<KT, VT>(p, smem, bar_full, bar_empty, abort, a, b, s, g, j);
+    consume_hg<KT, VT>(p, smem, bar_full, bar_empty, abort, a, b, s, g, j);
   } else {
     consume_shared<KT, VT, NT>(p, smem, bar_full, bar_empty, abort, a, b, s, g, j);
   }

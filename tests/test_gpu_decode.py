@@ -218,12 +218,16 @@ def test_bounded_wait_expires_with_status():
 
 
 def test_plan_covers_every_tile():
+    """One query token: 16-key tiles of all four KV heads (one segment per
+    sequence); more tokens: 64-key tiles of one head (four per sequence)."""
     w = W.config(3)
     from paged_kv_gqa_11_gb300.cache import PagedKVCache
     c = PagedKVCache(w.n_blocks, w.page_size, w.k_type, w.v_type)
-    plan = pa_decode_plan(c.pool, w.seq_lens, 1)
-    tiles = int(sum((L + 63) // 64 for L in w.seq_lens)) * W.HKV
-    assert plan["tiles"] == tiles and plan["tile_keys"] == 64
-    assert 0 < plan["ctas"] <= tiles
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    assert plan["ctas"] % sms == 0 or plan["ctas"] == tiles
+    for nq, keys, segs in ((1, 16, 1), (2, 64, W.HKV)):
+        plan = pa_decode_plan(c.pool, w.seq_lens, nq)
+        tiles = int(sum((L + keys - 1) // keys for L in w.seq_lens)) * segs
+        assert plan["tiles"] == tiles and plan["tile_keys"] == keys, (nq, plan)
+        assert 0 < plan["ctas"] <= tiles
+        assert plan["ctas"] % sms == 0 or plan["ctas"] == tiles
+        assert plan["partials"] >= w.n_seq * segs
