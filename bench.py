@@ -192,6 +192,21 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def rank_max(dist, x: float, device) -> float:
+    """The largest of one float over all ranks (the slowest rank's time)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbps(n_ranks: int, bytes_per_rank_step: int, slowest_step_ms: float) -> float:
+    """Whole-job K/V GB/s: every rank decodes its own batch (weak scaling)."""
+    return n_ranks * bytes_per_rank_step / (slowest_step_ms * 1e-3) / 1e9
+
+
 def _select(w: W.Workload, pairs):
     sel = np.zeros((w.n_seq, W.HQ), bool)
     for s, g in pairs:
@@ -436,18 +451,11 @@ def main():
         raise SystemExit("non-finite output")
 
     # ---- max over ranks
-    def rank_max(x):
-        if dist is None:
-            return x
-        tt = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        return float(tt.item())
-
-    step = rank_max(my_step)
-    split = rank_max(my_split)
-    e2e = rank_max(my_e2e)
+    step = rank_max(dist, my_step, dev)
+    split = rank_max(dist, my_split, dev)
+    e2e = rank_max(dist, my_e2e, dev)
     n = world
-    value = n * kv_bytes / (step * 1e-3) / 1e9
+    value = job_gbps(n, kv_bytes, step)
     achieved = kv_bytes / (split * 1e-3) / 1e9
     peaks = measured_peaks()
     peak = float(peaks["hbm_gbs"]) if peaks and "hbm_gbs" in peaks else FALLBACK_HBM_GBS
