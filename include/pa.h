@@ -217,6 +217,31 @@ pa_status pa_decode_plan(const pa_pool* pool, const int32_t* seq_lens_host, uint
                          uint32_t n_qtok, int device, uint32_t* n_ctas, uint32_t* n_tiles,
                          uint32_t* tile_keys, uint32_t* n_partials);
 
+/* ------------------------------------------------------------------ decode without allocation
+ * The pages describe no counterpart of this call; it exists for users of this
+ * library.  pa_decode_noalloc is pa_decode without the workspace arguments:
+ * its scratch is a fixed array of PA_NOALLOC_SCRATCH_BYTES bytes that the
+ * library reserves (as a static device variable) on every GPU that loads it,
+ * until the process exits.  It is meant for callers that cannot allocate
+ * device memory: code running under a memory budget fixed at start-up, hot
+ * loops that must avoid cudaMalloc's implicit synchronisation, plain C callers
+ * without an allocator.  It allocates nothing and calls no allocating routine.
+ *
+ * Arguments, results and device errors are those of pa_decode.  A batch whose
+ * workspace (pa_decode_workspace_size) exceeds PA_NOALLOC_SCRATCH_BYTES is
+ * refused with PA_ERR_UNSUPPORTED before anything is launched.  The first call
+ * on a device looks up the array's device address (once per device); make
+ * that first call before any stream capture.  All calls share the one array:
+ * calls whose work overlaps on the GPU race and must be serialised by the
+ * caller.  The array keeps the previous call's contents; the call needs no
+ * clearing. */
+#define PA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+pa_status pa_decode_noalloc(const pa_pool* pool, const float* q, const void* k_pool, const void* v_pool,
+                            const int32_t* block_table, uint32_t table_stride, const int32_t* seq_lens_dev,
+                            const int32_t* seq_lens_host, uint32_t n_seq, uint32_t n_qtok, uint32_t n_q_heads,
+                            float scale, float* out, float* lse, int32_t* err, pa_stream_t stream);
+
 /* ------------------------------------------------------------------ errors */
 
 /* Synchronise `stream`, read the device error word, reset it to 0 and return

@@ -20,7 +20,7 @@ from . import _build
 __all__ = [
     "PA_F16", "PA_Q4_0", "PA_Q8_0", "PaError", "Pool", "load", "row_bytes", "pa_append_rows", "pa_decode",
     "pa_decode_workspace_size", "pa_decode_plan", "pa_get_error", "pa_selftest_wait_timeout", "status_name",
-    "library_path",
+    "library_path", "pa_decode_noalloc",
 ]
 
 PA_F16, PA_Q4_0, PA_Q8_0 = 1, 2, 8
@@ -32,7 +32,7 @@ PA_OK, PA_ERR_INVALID, PA_ERR_UNSUPPORTED, PA_ERR_OOM, PA_ERR_STALE, PA_ERR_BOUN
 EXPORTS = ["pa_pool_create", "pa_pool_destroy", "pa_pool_get_desc", "pa_row_bytes", "pa_pool_bytes",
            "pa_alloc_blocks", "pa_release", "pa_block_index", "pa_pool_free_count", "pa_append_rows",
            "pa_decode", "pa_decode_split", "pa_decode_merge", "pa_decode_workspace_size", "pa_decode_plan", "pa_get_error", "pa_status_string",
-           "pa_selftest_wait_timeout"]
+           "pa_selftest_wait_timeout", "pa_decode_noalloc"]
 
 
 class PaError(RuntimeError):
@@ -88,6 +88,8 @@ def load():
             "pa_get_error": (C.c_int, [vp, vp]),
             "pa_status_string": (C.c_char_p, [C.c_int]),
             "pa_selftest_wait_timeout": (C.c_int, [u32, vp, vp]),
+            "pa_decode_noalloc": (C.c_int, [vp, vp, vp, vp, vp, u32, vp, vp, u32, u32, u32, C.c_float, vp, vp,
+                                            vp, vp]),
         }
         sig["pa_decode_split"] = sig["pa_decode_merge"] = sig["pa_decode"]
         for name, (res, args) in sig.items():
@@ -224,3 +226,16 @@ def pa_get_error(err, stream=None) -> int:
 
 def pa_selftest_wait_timeout(timeout_us: int, err, stream=None) -> int:
     return int(load().pa_selftest_wait_timeout(timeout_us, _ptr(err), _stream(stream)))
+
+
+NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
+
+
+def pa_decode_noalloc(pool: Pool, q, k_pool, v_pool, block_table, table_stride: int, seq_lens_dev, seq_lens_host,
+                      n_seq: int, n_qtok: int, n_q_heads: int, scale: float, out, lse, err, stream=None) -> int:
+    """pa_decode with the library's fixed scratch instead of a caller workspace
+    (for callers that cannot allocate device memory); returns the status."""
+    return int(load().pa_decode_noalloc(pool.handle, _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table),
+                                        table_stride, _ptr(seq_lens_dev), _ptr(seq_lens_host), n_seq, n_qtok,
+                                        n_q_heads, C.c_float(scale), _ptr(out), _ptr(lse), _ptr(err),
+                                        _stream(stream)))

@@ -566,3 +566,64 @@ extern "C" pa_status pa_decode(PA_DECODE_ARGS) { return run_decode(3, PA_DECODE_
 extern "C" pa_status pa_decode_split(PA_DECODE_ARGS) { return run_decode(1, PA_DECODE_FWD, stream); }
 
 extern "C" pa_status pa_decode_merge(PA_DECODE_ARGS) { return run_decode(2, PA_DECODE_FWD, stream); }
+
+// ------------------------------------------------------------------ decode without allocation
+//
+// pa_decode_noalloc is pa_decode for callers that cannot hand over a device
+// workspace: code that runs under a device-memory budget fixed at start-up
+// (any later cudaMalloc is refused or is a policy violation), hot loops that
+// must not pay cudaMalloc's implicit device synchronisation, and plain C
+// callers with no allocator of their own.  Its scratch is this file-scope
+// array, reserved on every GPU that loads the library until the process ends.
+//
+// `pa_noalloc_scratch` names a host-side stand-in in host code, not a device
+// address, so the kernels are given the address cudaGetSymbolAddress returns.
+// That lookup runs once per device, with the device current, on the first
+// call there; the first call on a device should therefore come before any
+// stream capture.  Every call shares the array and it keeps the last call's
+// contents; the split kernel zeroes the merge counters itself, and partials
+// are written before they are read, so nothing has to be cleared between
+// calls.  Each GPU has its own copy of the array; calls whose work overlaps on
+// one GPU (for example on two streams) race on it and must be serialised.
+static __device__ __align__(256) uint8_t pa_noalloc_scratch[PA_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[kMaxDevices];
+}  // namespace
+
+extern "C" pa_status pa_decode_noalloc(const pa_pool* pool, const float* q, const void* k_pool, const void* v_pool,
+                                       const int32_t* block_table, uint32_t table_stride,
+                                       const int32_t* seq_lens_dev, const int32_t* seq_lens_host, uint32_t n_seq,
+                                       uint32_t n_qtok, uint32_t n_q_heads, float scale, float* out, float* lse,
+                                       int32_t* err, pa_stream_t stream) {
+  if (!pool) return PA_ERR_INVALID;
+  if (n_seq == 0) {
+    pa_pool_desc d;
+    return check_shape(pool, n_qtok, n_q_heads, &d);
+  }
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return PA_ERR_CUDA;
+  if (device < 0 || device >= kMaxDevices) return PA_ERR_UNSUPPORTED;
+  // The scratch must hold this batch's workspace (an upper bound that does
+  // not depend on the sequence lengths); larger batches are refused.
+  const size_t need = pa_decode_workspace_size(pool, n_seq, n_qtok, device);
+  if (need == 0) {
+    pa_pool_desc d;
+    const pa_status st = check_shape(pool, n_qtok, n_q_heads, &d);
+    return st != PA_OK ? st : PA_ERR_UNSUPPORTED;
+  }
+  if (need > (size_t)PA_NOALLOC_SCRATCH_BYTES) return PA_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    if (!g_scratch_ptr[device]) {
+      void* ptr = nullptr;
+      if (cudaGetSymbolAddress(&ptr, pa_noalloc_scratch) != cudaSuccess || !ptr) return PA_ERR_CUDA;
+      g_scratch_ptr[device] = ptr;
+    }
+    scratch = g_scratch_ptr[device];
+  }
+  return run_decode(3, pool, q, k_pool, v_pool, block_table, table_stride, seq_lens_dev, seq_lens_host, n_seq,
+                    n_qtok, n_q_heads, scale, out, lse, scratch, (size_t)PA_NOALLOC_SCRATCH_BYTES, err, stream);
+}
