@@ -45,7 +45,8 @@ FALLBACK_HBM_GBS = 6800.0
 PAGES_PAGED_3090_MS = 4.095
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_split_ragged_q4_0.md")
 DECODE_SOURCES = ["paged_kv_gqa_11_gb300/csrc/pa_decode.cu", "paged_kv_gqa_11_gb300/csrc/pa_decode_impl.cuh",
-                  "paged_kv_gqa_11_gb300/csrc/pa_decode_kern_q4_0.cu", "paged_kv_gqa_11_gb300/csrc/pa_device.cuh"]
+                  "paged_kv_gqa_11_gb300/csrc/pa_decode_kern_q4_0.cu", "paged_kv_gqa_11_gb300/csrc/pa_device.cuh",
+                  "paged_kv_gqa_11_gb300/csrc/pa_layout.cuh"]
 
 
 def workload_for(name: str) -> W.Workload:

@@ -20,14 +20,24 @@
  *   - No call allocates device memory.  Scratch space for pa_decode is passed
  *     in by the caller, sized by pa_decode_workspace_size().
  *
- * Data layout (a reading of the pages; they describe a pool of pages plus a
- * page table but print no byte layout):
+ * Data layout.  The pages describe a pool of pages plus a page table but
+ * print no byte layout; this one is the library's own:
  *   K pool and V pool are separate device buffers, each
- *       pool[block][kv_head][slot][row_bytes]
- *   with slot in [0, page_size).  Row (seq s, position p) of kv head g lives
- *   in block block_table[s * table_stride + p / page_size] at slot
- *   p % page_size.  Each (block, kv_head) run of page_size rows is contiguous,
- *   so a page is copied with one bulk transfer per head.
+ *       pool[block][kv_head][page_size rows]
+ *   with page_size a multiple of 16.  Row (seq s, position p) of kv head g
+ *   lives in block block_table[s * table_stride + p / page_size] at slot
+ *   p % page_size.  Each (block, kv_head) page is cut into row groups of 16
+ *   consecutive slots; a group holds its 16 rows in 16 * row_bytes bytes,
+ *   arranged for the decode kernel's tensor-core fragment loads:
+ *     1. Q4_0/Q8_0 only: the rows' block scales (2 bytes each) in a 256-byte
+ *        scale region.  K pool: scale of (row r, block b) at 16 r + 2 b.
+ *        V pool: at 64 (b/2) + 16 ((r%8)/2) + 8 (b%2) + 4 (r/8) + 2 (r%2).
+ *     2. The rest of each row -- an F16 row, or a quantised row's quant bytes
+ *        block after block -- as 16-byte chunks, row after row; with C chunks
+ *        per row, chunk c of row r sits at chunk position r C + (c XOR r%8).
+ *   A row group is therefore one contiguous run that one bulk copy moves, and
+ *   a whole 16-row page of every head is one run per pool.  Write pools with
+ *   pa_append_rows, which takes rows in their ordinary format.
  *   Row formats are ggml's: F16 (IEEE binary16, 2*head_dim bytes), Q8_0
  *   (32-value blocks: fp16 scale d, 32 int8 q, value q*d; 34 bytes) and Q4_0
  *   (32-value blocks: fp16 d, 16 bytes whose byte j holds element j in the low
@@ -62,9 +72,9 @@ typedef enum { PA_F16 = 1, PA_Q4_0 = 2, PA_Q8_0 = 8 } pa_type;
 
 typedef struct {
   uint32_t n_blocks;   /* blocks in the pool, 1 .. 2^31-1 */
-  uint32_t page_size;  /* positions (rows) per block, >= 1 */
+  uint32_t page_size;  /* positions (rows) per block, a multiple of 16 */
   uint32_t n_kv_heads; /* KV heads per row */
-  uint32_t head_dim;   /* values per row; multiple of 32 */
+  uint32_t head_dim;   /* values per row; 256 */
   int32_t k_type;      /* pa_type of K rows */
   int32_t v_type;      /* pa_type of V rows */
 } pa_pool_desc;
@@ -82,8 +92,9 @@ typedef struct pa_pool pa_pool;
  * per pool). */
 
 /* Create a pool's allocator state.  PA_ERR_INVALID for a zero or oversize
- * field, PA_ERR_UNSUPPORTED for an unknown type.  *out is owned by the
- * caller and freed with pa_pool_destroy. */
+ * field, PA_ERR_UNSUPPORTED for an unknown type, a head_dim other than 256 or
+ * a page_size that is not a multiple of 16.  *out is owned by the caller and
+ * freed with pa_pool_destroy. */
 pa_status pa_pool_create(const pa_pool_desc* desc, pa_pool** out);
 
 /* Free the allocator state (not the device pools).  NULL is ignored. */

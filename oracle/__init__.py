@@ -38,6 +38,8 @@ _lock = threading.Lock()
 _lib = None
 
 F16, Q4_0, Q8_0 = 1, 2, 8
+ROLE_K, ROLE_V = 0, 1
+GROUP = 16  # slots per row group of the pool layout
 
 
 def build(force: bool = False) -> str:
@@ -101,8 +103,10 @@ def _load(path):
     L.orc_decode.argtypes = [C.POINTER(_Cache), C.c_void_p, C.c_double, C.c_void_p, C.c_void_p,
                              C.c_void_p, C.c_int]
     L.orc_scatter.restype = C.c_int
-    L.orc_scatter.argtypes = [C.c_void_p, C.c_long, C.c_int, C.c_int, C.c_long, C.c_void_p,
-                              C.c_void_p, C.c_void_p, C.c_long, C.c_void_p, C.c_long, C.c_int]
+    L.orc_scatter.argtypes = [C.c_void_p, C.c_long, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int,
+                              C.c_void_p, C.c_void_p, C.c_void_p, C.c_long, C.c_void_p, C.c_long, C.c_int]
+    L.orc_group_offset.restype = C.c_long
+    L.orc_group_offset.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int, C.c_long]
     return L
 
 
@@ -155,15 +159,23 @@ def dequant_rows(rows: np.ndarray, t: int, d: int = 256) -> np.ndarray:
     return out.reshape(*rows.shape[:-1], d)
 
 
-def scatter(pool: np.ndarray, n_blocks: int, hkv: int, page_size: int, rows: np.ndarray,
-            row_seq: np.ndarray, row_pos: np.ndarray, table: np.ndarray) -> int:
-    """Write packed rows [n][hkv][rb] into `pool` (uint8, modified in place)."""
+def group_offset(t: int, role: int, r: int, i: int, d: int = 256) -> int:
+    """Byte offset, inside its 16-row group, of byte i of the row stored in
+    group row r (-1 outside the layout)."""
+    return int(lib().orc_group_offset(t, role, d, r, i))
+
+
+def scatter(pool: np.ndarray, n_blocks: int, hkv: int, page_size: int, t: int, role: int,
+            rows: np.ndarray, row_seq: np.ndarray, row_pos: np.ndarray, table: np.ndarray,
+            d: int = 256) -> int:
+    """Write packed rows [n][hkv][rb] of format t into a pool of the given role
+    (uint8, modified in place)."""
     rows = np.ascontiguousarray(rows, dtype=np.uint8)
     rs = np.ascontiguousarray(row_seq, dtype=np.int32)
     rp = np.ascontiguousarray(row_pos, dtype=np.int32)
     tab = np.ascontiguousarray(table, dtype=np.int32)
     assert pool.flags.c_contiguous and pool.dtype == np.uint8
-    return int(lib().orc_scatter(_ptr(pool), n_blocks, hkv, page_size, rows.shape[-1], _ptr(rows),
+    return int(lib().orc_scatter(_ptr(pool), n_blocks, hkv, page_size, t, role, d, _ptr(rows),
                                  _ptr(rs), _ptr(rp), rows.shape[0], _ptr(tab), tab.shape[1],
                                  tab.shape[0]))
 
@@ -191,8 +203,9 @@ class Cache:
         kp = np.zeros(nb * hkv * w.page_size * rbk, np.uint8)
         vp = np.zeros(nb * hkv * w.page_size * rbv, np.uint8)
         rs, rp = w.row_seq, w.row_pos
-        rc = scatter(kp, nb, hkv, w.page_size, w.k_rows, rs, rp, tab)
-        rc |= scatter(vp, nb, hkv, w.page_size, w.v_rows, rs, rp, tab)
+        d = w.q.shape[3]
+        rc = scatter(kp, nb, hkv, w.page_size, w.k_type, ROLE_K, w.k_rows, rs, rp, tab, d)
+        rc |= scatter(vp, nb, hkv, w.page_size, w.v_type, ROLE_V, w.v_rows, rs, rp, tab, d)
         if rc:
             raise ValueError(f"scatter rc={rc}")
         return cls(w.seq_lens, w.n_qtok, w.page_size, nb, w.k_type, w.v_type, tab, kp, vp,

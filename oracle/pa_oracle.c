@@ -20,8 +20,9 @@
  *    logical page is either a pool page ..." (llama.cpp fork PR #2,
  *    ggml_flash_attn_ext_set_pages commit); every row address comes from the
  *    table, the page stride and the positions per page (TensorFold #1156,
- *    Design / Kernels, kv_row()).  Pool layout (a reading):
- *    pool[block][kv_head][slot][row_bytes].
+ *    Design / Kernels, kv_row()).  Which bytes of the pool hold a row is this
+ *    library's own choice (the pages print no byte layout); it is written out
+ *    in orc_group_offset below.
  *
  *  - Attention.  Query head h uses KV head h / (Hq/Hkv) ("GQA 6", llama.cpp
  *    fork PR #2, split-K decode commit; contiguous grouping is a reading).
@@ -41,7 +42,7 @@
  *
  *  - Scatter (append): row (seq, pos) goes to block table[seq][pos/ps], slot
  *    pos%ps (colibri PR #372, Summary: upload new rows, scatter them into
- *    their page slots).
+ *    their page slots), its bytes placed as orc_group_offset says.
  */
 #include <math.h>
 #include <stdint.h>
@@ -56,6 +57,10 @@
 #define ORC_ERR_ARG (-1)
 #define ORC_ERR_BOUNDS (-2)
 #define ORC_ERR_NOMEM (-3)
+
+#define ORC_ROLE_K 0
+#define ORC_ROLE_V 1
+#define ORC_GROUP 16
 
 /* IEEE 754 binary16 -> double, from the format definition:
  * 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
@@ -112,6 +117,49 @@ int orc_dequant_row(int type, const uint8_t* row, int d, double* out) {
   return ORC_OK;
 }
 
+/* Pool layout.  A pool is [block][kv_head][page_size rows] with page_size a
+ * multiple of ORC_GROUP (16); each page is cut into groups of 16 consecutive
+ * slots, and a group stores its 16 rows in 16 * row_bytes bytes, arranged for
+ * the decode kernel's tensor-core fragment loads instead of row after row:
+ *
+ *   1. Quantised formats (Q4_0, Q8_0) first keep the block scales of the 16
+ *      rows, 2 bytes each, in a region of 32 * nb bytes (nb = d / 32 blocks
+ *      per row).  In a K pool the scale of (row r, block b) sits at byte
+ *      2 * (r * nb + b).  In a V pool it sits at
+ *        64 * (b / 2) + 16 * ((r % 8) / 2) + 8 * (b % 2) + 4 * (r / 8) + 2 * (r % 2).
+ *   2. The rest of every row (all of an F16 row; the quant bytes of a Q4_0 or
+ *      Q8_0 row, block after block) follows as 16-byte chunks, row 0 first.
+ *      With C chunks per row, chunk c of row r is stored at chunk position
+ *      r * C + (c XOR (r % 8)).
+ *
+ * Returns the byte offset within the group of byte i (0 <= i < row_bytes) of
+ * the row stored in group row r, or -1 for an argument outside the layout. */
+long orc_group_offset(int type, int role, int d, int r, long i) {
+  const long rb = orc_row_bytes(type, d);
+  if (rb < 0 || r < 0 || r >= ORC_GROUP || i < 0 || i >= rb) return -1;
+  if (role != ORC_ROLE_K && role != ORC_ROLE_V) return -1;
+  const int nb = d / 32;
+  if (type == ORC_F16) {
+    const long chunks = rb / 16;
+    if (chunks % 8) return -1;
+    const long c = i / 16;
+    return (r * chunks + (c ^ (r % 8))) * 16 + i % 16;
+  }
+  const long bb = (type == ORC_Q4_0) ? 18 : 34; /* bytes per 32-value block */
+  const long b = i / bb, o = i % bb;
+  if (o < 2) { /* scale byte o of block b */
+    if (role == ORC_ROLE_K) return 2L * (r * nb + b) + o;
+    if (nb % 2) return -1;
+    return 64 * (b / 2) + 16 * ((r % 8) / 2) + 8 * (b % 2) + 4 * (r / 8) + 2 * (r % 2) + o;
+  }
+  const long per_row = nb * (bb - 2); /* quant bytes per row */
+  const long chunks = per_row / 16;
+  if (chunks % 8) return -1;
+  const long qi = b * (bb - 2) + (o - 2); /* index among the row's quant bytes */
+  const long c = qi / 16;
+  return 32L * nb + (r * chunks + (c ^ (r % 8))) * 16 + qi % 16;
+}
+
 /* Geometry of one paged cache. */
 typedef struct {
   int n_seq, n_qtok, hq, hkv, d, page_size;
@@ -124,16 +172,21 @@ typedef struct {
   const uint8_t* v_pool;
 } orc_cache;
 
-/* Address of row `pos` of sequence s, KV head g, or NULL when the table entry
- * is outside the pool. */
-static const uint8_t* row_addr(const orc_cache* c, const uint8_t* pool, long rb, int s, int g,
-                               long pos) {
+/* Copy row `pos` of sequence s, KV head g out of a pool (role K or V) into
+ * out[0..row_bytes) in the row's own format.  ORC_ERR_BOUNDS when the position
+ * is past the table or the table entry is outside the pool. */
+static int fetch_row(const orc_cache* c, int role, int s, int g, long pos, uint8_t* out) {
+  const int type = role == ORC_ROLE_K ? c->k_type : c->v_type;
+  const uint8_t* pool = role == ORC_ROLE_K ? c->k_pool : c->v_pool;
+  const long rb = orc_row_bytes(type, c->d);
   long page = pos / c->page_size;
   long slot = pos % c->page_size;
-  if (page >= c->table_stride) return NULL;
+  if (page >= c->table_stride) return ORC_ERR_BOUNDS;
   long blk = c->table[(long)s * c->table_stride + page];
-  if (blk < 0 || blk >= c->n_blocks) return NULL;
-  return pool + (((blk * c->hkv + g) * (long)c->page_size + slot) * rb);
+  if (blk < 0 || blk >= c->n_blocks) return ORC_ERR_BOUNDS;
+  const uint8_t* grp = pool + ((blk * c->hkv + g) * (long)c->page_size + slot / ORC_GROUP * ORC_GROUP) * rb;
+  for (long i = 0; i < rb; ++i) out[i] = grp[orc_group_offset(type, role, c->d, (int)(slot % ORC_GROUP), i)];
+  return ORC_OK;
 }
 
 /* Plain attention over keys [j0, j1) of sequence s for query (t, h):
@@ -157,13 +210,14 @@ int orc_attend_range(const orc_cache* c, const float* q, double scale, int s, in
   long n = j1 - j0;
   double* z = (double*)malloc(sizeof(double) * n);
   double* row = (double*)malloc(sizeof(double) * d);
-  if (!z || !row) { free(z); free(row); return ORC_ERR_NOMEM; }
+  uint8_t* bytes = (uint8_t*)malloc((size_t)(rbk > rbv ? rbk : rbv));
+  if (!z || !row || !bytes) { free(z); free(row); free(bytes); return ORC_ERR_NOMEM; }
   int rc = ORC_OK;
   double m = -INFINITY;
   for (long j = j0; j < j1 && rc == ORC_OK; ++j) {
-    const uint8_t* kr = row_addr(c, c->k_pool, rbk, s, g, j);
-    if (!kr) { rc = ORC_ERR_BOUNDS; break; }
-    orc_dequant_row(c->k_type, kr, d, row);
+    rc = fetch_row(c, ORC_ROLE_K, s, g, j, bytes);
+    if (rc != ORC_OK) break;
+    orc_dequant_row(c->k_type, bytes, d, row);
     double acc = 0.0;
     for (int i = 0; i < d; ++i) acc += (double)qv[i] * row[i];
     z[j - j0] = scale * acc;
@@ -171,9 +225,9 @@ int orc_attend_range(const orc_cache* c, const float* q, double scale, int s, in
   }
   double l = 0.0;
   for (long j = j0; j < j1 && rc == ORC_OK; ++j) {
-    const uint8_t* vr = row_addr(c, c->v_pool, rbv, s, g, j);
-    if (!vr) { rc = ORC_ERR_BOUNDS; break; }
-    orc_dequant_row(c->v_type, vr, d, row);
+    rc = fetch_row(c, ORC_ROLE_V, s, g, j, bytes);
+    if (rc != ORC_OK) break;
+    orc_dequant_row(c->v_type, bytes, d, row);
     double w = exp(z[j - j0] - m);
     l += w;
     for (int i = 0; i < d; ++i) o[i] += w * row[i];
@@ -187,6 +241,7 @@ int orc_attend_range(const orc_cache* c, const float* q, double scale, int s, in
   }
   free(z);
   free(row);
+  free(bytes);
   return rc;
 }
 
@@ -215,7 +270,8 @@ void orc_merge(int n_parts, const double* m, const double* l, const double* o, i
  * (seq, q-head) when compiled with it. */
 int orc_decode(const orc_cache* c, const float* q, double scale, const uint8_t* sel,
                double* out, double* lse, int n_threads) {
-  if (!c || c->hkv <= 0 || c->hq % c->hkv || c->page_size <= 0 || c->n_qtok <= 0) return ORC_ERR_ARG;
+  if (!c || c->hkv <= 0 || c->hq % c->hkv || c->page_size <= 0 || c->page_size % ORC_GROUP || c->n_qtok <= 0)
+    return ORC_ERR_ARG;
   if (orc_row_bytes(c->k_type, c->d) < 0 || orc_row_bytes(c->v_type, c->d) < 0) return ORC_ERR_ARG;
   const long npairs = (long)c->n_seq * c->hq;
   int rc_all = ORC_OK;
@@ -242,11 +298,16 @@ int orc_decode(const orc_cache* c, const float* q, double scale, const uint8_t* 
   return rc_all;
 }
 
-/* Scatter n_rows packed rows ([n][hkv][rb]) into a pool through the table.
- * Returns ORC_ERR_BOUNDS (and skips the row) for an entry outside the pool. */
-int orc_scatter(uint8_t* pool, long n_blocks, int hkv, int page_size, long rb, const uint8_t* rows,
-                const int32_t* row_seq, const int32_t* row_pos, long n_rows, const int32_t* table,
-                long table_stride, int n_seq) {
+/* Scatter n_rows packed rows ([n][hkv][rb], row format `type`) into a pool
+ * (role K or V) through the table, placing each row's bytes as
+ * orc_group_offset says.  Returns ORC_ERR_BOUNDS (and skips the row) for a
+ * position past the table or an entry outside the pool. */
+int orc_scatter(uint8_t* pool, long n_blocks, int hkv, int page_size, int type, int role, int d,
+                const uint8_t* rows, const int32_t* row_seq, const int32_t* row_pos, long n_rows,
+                const int32_t* table, long table_stride, int n_seq) {
+  const long rb = orc_row_bytes(type, d);
+  if (rb < 0 || page_size <= 0 || page_size % ORC_GROUP) return ORC_ERR_ARG;
+  if (orc_group_offset(type, role, d, 0, 0) < 0) return ORC_ERR_ARG;
   int rc = ORC_OK;
   for (long i = 0; i < n_rows; ++i) {
     int s = row_seq[i];
@@ -254,9 +315,12 @@ int orc_scatter(uint8_t* pool, long n_blocks, int hkv, int page_size, long rb, c
     if (s < 0 || s >= n_seq || pos < 0 || pos / page_size >= table_stride) { rc = ORC_ERR_BOUNDS; continue; }
     long blk = table[(long)s * table_stride + pos / page_size];
     if (blk < 0 || blk >= n_blocks) { rc = ORC_ERR_BOUNDS; continue; }
-    for (int g = 0; g < hkv; ++g)
-      memcpy(pool + ((blk * hkv + g) * (long)page_size + pos % page_size) * rb,
-             rows + (i * hkv + g) * rb, (size_t)rb);
+    long slot = pos % page_size;
+    for (int g = 0; g < hkv; ++g) {
+      uint8_t* grp = pool + ((blk * hkv + g) * (long)page_size + slot / ORC_GROUP * ORC_GROUP) * rb;
+      const uint8_t* src = rows + (i * hkv + g) * rb;
+      for (long b = 0; b < rb; ++b) grp[orc_group_offset(type, role, d, (int)(slot % ORC_GROUP), b)] = src[b];
+    }
   }
   return rc;
 }

@@ -2,21 +2,24 @@
 //
 // colibri PR #372 (Summary): "upload only newly appended KV rows through one
 // packed transfer and scatter kernel".  The caller uploads the new rows once,
-// packed as [n_rows][n_kv_heads][row_bytes]; this kernel copies each (row,
-// head) to pool[block][head][slot] with block = table[seq][pos / page_size]
-// and slot = pos % page_size.  The copy is byte-exact (rows are already in
-// storage format) and moves 16-byte vectors: every row size of the supported
-// formats (F16 512, Q4_0 144, Q8_0 272 bytes per 256 values) is a multiple of
-// 16, so each thread moves one aligned uint4 and a warp covers consecutive
-// chunks of consecutive rows.
+// packed as [n_rows][n_kv_heads][row_bytes] in their ggml format; this kernel
+// places each (row, head) in block table[seq][pos / page_size], slot
+// pos % page_size, arranging its bytes in the pool's row-group layout
+// (pa_layout.cuh): quant bytes as 16-byte chunks at their swizzled chunk
+// positions, block scales in the group's scale region.  One thread moves one
+// 32-value block of a quantised row (one 16- or two 32-byte chunk stores and a
+// 2-byte scale) or one 16-byte chunk of an F16 row; a warp covers consecutive
+// units of consecutive rows.
 #include <cuda_runtime.h>
 
 #include <cstdint>
 
 #include "pa.h"
 #include "pa_device.cuh"
+#include "pa_layout.cuh"
 
 using namespace pa_dev;
+using namespace pa_layout;
 
 namespace {
 
@@ -35,38 +38,68 @@ struct AppendParams {
   int table_stride;
   int n_seq;
   int n_blocks;
-  int k_chunks;  // 16-byte chunks per K row
-  int v_chunks;
+  int k_type, v_type;
+  int k_units, v_units;  // units per row: 32 chunks (F16) or 8 blocks
+  int k_row, v_row;      // row bytes
 };
 
-// One thread per 16-byte chunk of the packed input; K chunks first, then V.
+__device__ __forceinline__ uint32_t ld_u16(const uint8_t* p) { return *reinterpret_cast<const uint16_t*>(p); }
+
+// Move unit u of a row (src, ggml format) into its group (dst = group base,
+// r = row in the group).  role_v selects the V scale arrangement.
+__device__ __forceinline__ void place_unit(int type, bool role_v, const uint8_t* src, uint8_t* grp, int r, int u) {
+  if (type == PA_F16) {
+    const uint4 v = *reinterpret_cast<const uint4*>(src + 16 * u);
+    *reinterpret_cast<uint4*>(grp + chunk_offset(0, Fmt<PA_F16>::kRowQ, r, u)) = v;
+    return;
+  }
+  const bool q4 = type == PA_Q4_0;
+  const uint8_t* blk = src + (q4 ? 18 : 34) * u;  // 2-byte aligned
+  const uint32_t d = ld_u16(blk);
+  const int n_chunks = q4 ? 1 : 2;
+  for (int c = 0; c < n_chunks; ++c) {
+    const uint8_t* q = blk + 2 + 16 * c;
+    uint4 v;
+    v.x = ld_u16(q + 0) | (ld_u16(q + 2) << 16);
+    v.y = ld_u16(q + 4) | (ld_u16(q + 6) << 16);
+    v.z = ld_u16(q + 8) | (ld_u16(q + 10) << 16);
+    v.w = ld_u16(q + 12) | (ld_u16(q + 14) << 16);
+    const int chunk = q4 ? u : 2 * u + c;
+    *reinterpret_cast<uint4*>(grp + chunk_offset(256, q4 ? Fmt<PA_Q4_0>::kRowQ : Fmt<PA_Q8_0>::kRowQ, r, chunk)) = v;
+  }
+  *reinterpret_cast<uint16_t*>(grp + (role_v ? v_scale_offset(r, u) : k_scale_offset(r, u))) = (uint16_t)d;
+}
+
+// One thread per unit of the packed input; K units first, then V.
 __global__ void __launch_bounds__(256) pa_append_kernel(const __grid_constant__ AppendParams p) {
-  const long long k_total = p.n_rows * p.n_kv_heads * p.k_chunks;
-  const long long v_total = p.n_rows * p.n_kv_heads * p.v_chunks;
+  const long long k_total = p.n_rows * p.n_kv_heads * p.k_units;
+  const long long v_total = p.n_rows * p.n_kv_heads * p.v_units;
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < k_total + v_total; i += stride) {
     const bool is_k = i < k_total;
     const long long li = is_k ? i : i - k_total;
-    const int chunks = is_k ? p.k_chunks : p.v_chunks;
-    const long long rh = li / chunks;  // (row, head)
-    const int c = (int)(li - rh * chunks);
+    const int units = is_k ? p.k_units : p.v_units;
+    const long long rh = li / units;  // (row, head)
+    const int u = (int)(li - rh * units);
     const long long r = rh / p.n_kv_heads;
     const int h = (int)(rh - r * p.n_kv_heads);
     const int s = __ldg(p.row_seq + r);
     const int pos = __ldg(p.row_pos + r);
     if (s < 0 || s >= p.n_seq || pos < 0 || pos / p.page_size >= p.table_stride) {
-      if (c == 0 && h == 0 && is_k) record_error(p.err, PA_ERR_BOUNDS);
+      if (u == 0 && h == 0 && is_k) record_error(p.err, PA_ERR_BOUNDS);
       continue;
     }
     const int blk = __ldg(p.table + (long long)s * p.table_stride + pos / p.page_size);
     if (blk < 0 || blk >= p.n_blocks) {
-      if (c == 0 && h == 0 && is_k) record_error(p.err, PA_ERR_BOUNDS);
+      if (u == 0 && h == 0 && is_k) record_error(p.err, PA_ERR_BOUNDS);
       continue;
     }
-    const long long dst_row = ((long long)blk * p.n_kv_heads + h) * p.page_size + pos % p.page_size;
-    const uint4* src = reinterpret_cast<const uint4*>(is_k ? p.k_rows : p.v_rows) + li;
-    uint4* dst = reinterpret_cast<uint4*>(is_k ? p.k_pool : p.v_pool) + dst_row * chunks + c;
-    *dst = __ldg(src);
+    const int rb = is_k ? p.k_row : p.v_row;
+    const int slot = pos % p.page_size;
+    const long long grp_row = ((long long)blk * p.n_kv_heads + h) * p.page_size + (slot & ~(kGroup - 1));
+    uint8_t* grp = (is_k ? p.k_pool : p.v_pool) + grp_row * rb;
+    const uint8_t* src = (is_k ? p.k_rows : p.v_rows) + rh * rb;
+    place_unit(is_k ? p.k_type : p.v_type, !is_k, src, grp, slot & (kGroup - 1), u);
   }
 }
 
@@ -115,9 +148,13 @@ extern "C" pa_status pa_append_rows(const pa_pool* pool, void* k_pool, void* v_p
   p.table_stride = (int)table_stride;
   p.n_seq = (int)n_seq;
   p.n_blocks = (int)d.n_blocks;
-  p.k_chunks = (int)(rbk / 16);
-  p.v_chunks = (int)(rbv / 16);
-  const long long total = (long long)n_rows * d.n_kv_heads * (p.k_chunks + p.v_chunks);
+  p.k_type = (int)d.k_type;
+  p.v_type = (int)d.v_type;
+  p.k_units = d.k_type == PA_F16 ? (int)(rbk / 16) : (int)(d.head_dim / 32);
+  p.v_units = d.v_type == PA_F16 ? (int)(rbv / 16) : (int)(d.head_dim / 32);
+  p.k_row = (int)rbk;
+  p.v_row = (int)rbv;
+  const long long total = (long long)n_rows * d.n_kv_heads * (p.k_units + p.v_units);
   int device = 0, sms = 0;
   if (cudaGetDevice(&device) != cudaSuccess) return PA_ERR_CUDA;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return PA_ERR_CUDA;

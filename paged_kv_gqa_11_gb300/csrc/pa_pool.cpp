@@ -46,6 +46,9 @@ extern "C" pa_status pa_pool_create(const pa_pool_desc* desc, pa_pool** out) {
     return PA_ERR_INVALID;
   if (pa_row_bytes(desc->k_type, desc->head_dim) == 0 || pa_row_bytes(desc->v_type, desc->head_dim) == 0)
     return PA_ERR_UNSUPPORTED;
+  // The pool's row-group layout is defined for 256-value rows and pages of
+  // whole 16-row groups.
+  if (desc->head_dim != 256 || desc->page_size % 16 != 0) return PA_ERR_UNSUPPORTED;
   pa_pool* p = new (std::nothrow) pa_pool();
   if (!p) return PA_ERR_OOM;
   try {

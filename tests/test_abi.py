@@ -52,9 +52,10 @@ def test_pool_bytes_and_validation(lib):
         with pytest.raises(pa.PaError) as e:
             pa.Pool(bad[0], bad[1], 4, 256, pa.PA_F16)
         assert e.value.status == pa.PA_ERR_INVALID
-    with pytest.raises(pa.PaError) as e:
-        pa.Pool(8, 16, 4, 256, 5)
-    assert e.value.status == pa.PA_ERR_UNSUPPORTED
+    for bad in [(16, 256, 5), (8, 256, pa.PA_Q4_0), (24, 256, pa.PA_F16), (16, 128, pa.PA_F16)]:
+        with pytest.raises(pa.PaError) as e:
+            pa.Pool(8, bad[0], 4, bad[1], bad[2])  # bad type, page not whole groups, head_dim not 256
+        assert e.value.status == pa.PA_ERR_UNSUPPORTED
 
 
 def _random_ops(seed, n_blocks, steps):
@@ -119,8 +120,6 @@ def test_decode_rejects_unsupported_shapes_on_host(lib):
                 workspace=8192, ws_bytes=1 << 20, err=8192, stream=0, check=False)
     assert pa.pa_decode(ok, **{**args, "n_qtok": 5}) == pa.PA_ERR_UNSUPPORTED
     assert pa.pa_decode(ok, **{**args, "n_q_heads": 16}) == pa.PA_ERR_UNSUPPORTED
-    odd = pa.Pool(8, 16, 4, 128, pa.PA_F16)
-    assert pa.pa_decode(odd, **args) == pa.PA_ERR_UNSUPPORTED
     assert pa.pa_decode(ok, **{**args, "q": None}) == pa.PA_ERR_INVALID
     assert pa.pa_decode(ok, **{**args, "q": 8196}) == pa.PA_ERR_INVALID   # not 16-byte aligned
     assert pa.pa_decode(ok, **{**args, "n_seq": 0}) == pa.PA_OK

@@ -21,7 +21,7 @@ def oracle_pools(w):
 
 CASES = [
     ("f16-ps16", [300, 17], 16, W.TYPE_F16, W.TYPE_F16, "shuffled"),
-    ("q4-ps1", [40, 3], 1, W.TYPE_Q4_0, W.TYPE_Q4_0, "shuffled"),
+    ("q4-ps32", [40, 3], 32, W.TYPE_Q4_0, W.TYPE_Q4_0, "shuffled"),
     ("q8-ps48", [500, 96, 1], 48, W.TYPE_Q8_0, W.TYPE_Q8_0, "interleaved"),
     ("mixed-ps256", [700], 256, W.TYPE_Q8_0, W.TYPE_Q4_0, "shuffled"),
 ]
@@ -70,7 +70,7 @@ def test_append_bounds_guard():
     # expected: oracle scatter of the rows that had a valid entry only
     ko2 = np.zeros_like(ko)
     vo2 = np.zeros_like(vo)
-    oracle.scatter(ko2, w.n_blocks, 4, 16, w.k_rows[keep], w.row_seq[keep], w.row_pos[keep], good)
-    oracle.scatter(vo2, w.n_blocks, 4, 16, w.v_rows[keep], w.row_seq[keep], w.row_pos[keep], good)
+    oracle.scatter(ko2, w.n_blocks, 4, 16, w.k_type, oracle.ROLE_K, w.k_rows[keep], w.row_seq[keep], w.row_pos[keep], good)
+    oracle.scatter(vo2, w.n_blocks, 4, 16, w.v_type, oracle.ROLE_V, w.v_rows[keep], w.row_seq[keep], w.row_pos[keep], good)
     assert np.array_equal(c.k_pool.cpu().numpy(), ko2)
     assert np.array_equal(c.v_pool.cpu().numpy(), vo2)

@@ -30,10 +30,10 @@ F16, Q4, Q8 = W.TYPE_F16, W.TYPE_Q4_0, W.TYPE_Q8_0
 SMALL = [
     ("f16-1tok", [300], 16, F16, F16, 1, "shuffled"),
     ("q4-edges", [1, 63, 64, 65, 129], 16, Q4, Q4, 1, "shuffled"),
-    ("q8-ps3-2tok", [200, 7], 3, Q8, Q8, 2, "shuffled"),
+    ("q8-ps32-2tok", [200, 7], 32, Q8, Q8, 2, "shuffled"),
     ("q8-masked-4tok", [513, 64, 4], 256, Q8, Q8, 4, "shuffled"),
     ("f16-ps48-3tok", [1000, 130], 48, F16, F16, 3, "interleaved"),
-    ("q4-ps1-4tok", [777], 1, Q4, Q4, 4, "shuffled"),
+    ("q4-ps80-4tok", [777], 80, Q4, Q4, 4, "shuffled"),
     ("q4-mix-2tok", [2048, 333, 17, 4096], 64, Q4, Q4, 2, "shuffled"),
     ("q8-min-len", [1, 2, 3], 16, Q8, Q8, 1, "shuffled"),
     ("f16-min-len-4tok", [4, 5, 6, 67], 16, F16, F16, 4, "shuffled"),
@@ -115,7 +115,7 @@ def test_page_size_invariance_and_repeats():
     identical."""
     base = W.make_workload("inv", 77, [3000, 129, 1025], 16, Q4, Q4, 3, "identity")
     ref_o, ref_l = run_decode(base)
-    for ps in (1, 16, 48, 64, 256):
+    for ps in (16, 32, 48, 64, 80, 256):
         lists = W.interleaved_blocks(base.seq_lens, ps)
         n = sum(len(l) for l in lists)
         perm = np.random.default_rng(ps).permutation(n)

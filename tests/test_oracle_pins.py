@@ -26,7 +26,7 @@ def _golden(name):
 
 def workload_from_sources(lengths, ps, kt, vt, n_qtok, k_src, v_src, q, layout="shuffled", seed=0):
     """A workload whose rows are the given float sources (encoded per type)."""
-    base = W.make_workload("pin", seed, [1], 1, W.TYPE_F16, W.TYPE_F16, 1, "identity")
+    base = W.make_workload("pin", seed, [1], 16, W.TYPE_F16, W.TYPE_F16, 1, "identity")
     lengths = np.asarray(lengths, np.int32)
     rng = np.random.default_rng(seed + 1000)
     lists = W.interleaved_blocks(lengths, ps)
@@ -183,7 +183,7 @@ def pin_identical_keys_and_zero_query():
     k = np.tile(rng.standard_normal((1, HKV, D), dtype=np.float32), (L, 1, 1))
     v = rng.standard_normal((L, HKV, D), dtype=np.float32)
     q = rng.standard_normal((1, 1, HQ, D), dtype=np.float32)
-    w = workload_from_sources([L], 8, W.TYPE_F16, W.TYPE_F16, 1, k, v, q)
+    w = workload_from_sources([L], 16, W.TYPE_F16, W.TYPE_F16, 1, k, v, q)
     out, lse = oracle.decode_workload(w)
     vd = oracle.dequant_rows(w.v_rows, W.TYPE_F16)
     kd = oracle.dequant_rows(w.k_rows[:1], W.TYPE_F16)[0]
@@ -208,7 +208,7 @@ def pin_gqa_mapping():
     for g in range(HKV):
         v[:, g, :] = (g + 1) / 2
     q = rng.standard_normal((2, 1, HQ, D), dtype=np.float32)
-    w = workload_from_sources([L // 2, L // 2], 4, W.TYPE_Q8_0, W.TYPE_F16, 1, k, v, q)
+    w = workload_from_sources([L // 2, L // 2], 32, W.TYPE_Q8_0, W.TYPE_F16, 1, k, v, q)
     out, _ = oracle.decode_workload(w)
     for h in range(HQ):
         assert np.allclose(out[:, 0, h], (h // 6 + 1) / 2, rtol=1e-13), h
@@ -224,7 +224,7 @@ def pin_causal_verify():
         v[j] = j
     q = np.zeros((1, nq, HQ, D), np.float32)
     q[..., 0] = 2.0  # z = (1/16) * 2 * 0.5 = 1/16
-    w = workload_from_sources([L], 2, W.TYPE_F16, W.TYPE_F16, nq, k, v, q)
+    w = workload_from_sources([L], 16, W.TYPE_F16, W.TYPE_F16, nq, k, v, q)
     out, lse = oracle.decode_workload(w)
     for t in range(nq):
         assert np.allclose(out[0, t], (5 + t) / 2, rtol=1e-13), (t, out[0, t, 0, 0])
@@ -241,7 +241,7 @@ def pin_dominant_key():
         k[jstar, :, 0] = 8.0
         v = rng.standard_normal((L, HKV, D), dtype=np.float32)
         q = _onehot_q(1, 1, 0, 160.0)
-        w = workload_from_sources([L], 3, W.TYPE_F16, W.TYPE_Q8_0, 1, k, v, q)
+        w = workload_from_sources([L], 16, W.TYPE_F16, W.TYPE_Q8_0, 1, k, v, q)
         out, lse = oracle.decode_workload(w)
         vd = oracle.dequant_rows(w.v_rows, W.TYPE_Q8_0)
         for h in range(HQ):
@@ -274,10 +274,10 @@ def _dense_reference(w):
 
 
 def pin_dense_brute_force():
-    cases = [([7, 1, 20], 3, W.TYPE_F16, W.TYPE_F16, 1),
+    cases = [([7, 1, 20], 16, W.TYPE_F16, W.TYPE_F16, 1),
              ([33, 16], 16, W.TYPE_Q4_0, W.TYPE_Q4_0, 2),
-             ([5, 40], 7, W.TYPE_Q8_0, W.TYPE_Q8_0, 4),
-             ([18], 1, W.TYPE_Q8_0, W.TYPE_Q4_0, 3)]
+             ([5, 40], 32, W.TYPE_Q8_0, W.TYPE_Q8_0, 4),
+             ([18, 50], 48, W.TYPE_Q8_0, W.TYPE_Q4_0, 3)]
     for i, (lens, ps, kt, vt, nq) in enumerate(cases):
         w = W.make_workload("bf", 100 + i, lens, ps, kt, vt, nq, "shuffled")
         out, lse = oracle.decode_workload(w)
@@ -291,7 +291,7 @@ def pin_placement_and_page_size_invariance():
     (TensorFold #1156: paged == contiguous for any page size)."""
     base = W.make_workload("inv", 21, [45, 16, 70], 16, W.TYPE_Q4_0, W.TYPE_Q4_0, 2, "identity")
     ref_out, ref_lse = oracle.decode_workload(base)
-    for ps in (1, 3, 16, 48, 128):
+    for ps in (16, 32, 48, 128, 256):
         for layout in ("identity", "shuffled"):
             rng = np.random.default_rng(ps)
             lists = W.interleaved_blocks(base.seq_lens, ps)
@@ -310,7 +310,7 @@ def pin_split_merge():
     """Any partition of the visible keys, merged by log-sum-exp, equals the
     unsplit softmax (llama.cpp fork PR #2, LSE commit), over many random
     splittings, including empty (fully masked) parts."""
-    w = W.make_workload("sm", 31, [70, 9], 5, W.TYPE_Q8_0, W.TYPE_Q4_0, 3, "shuffled")
+    w = W.make_workload("sm", 31, [70, 9], 16, W.TYPE_Q8_0, W.TYPE_Q4_0, 3, "shuffled")
     cache = oracle.Cache.from_workload(w)
     full_out, full_lse = oracle.decode(cache, w.q, w.scale)
     rng = np.random.default_rng(7)
@@ -342,11 +342,58 @@ def pin_fully_masked_part():
     assert lse == -np.inf and np.array_equal(out, np.zeros(D))
 
 
+# ------------------------------------------------------------------ pool layout
+
+# Offsets worked out by hand from the written layout definition (pa.h, "Pool
+# layout"): (format, role, group row r, byte i of the row) -> byte in the group.
+LAYOUT_FIXTURES = [
+    (W.TYPE_Q4_0, oracle.ROLE_K, 0, 0, 0),        # scale of block 0, row 0
+    (W.TYPE_Q4_0, oracle.ROLE_K, 3, 37, 53),      # block 2 scale, high byte: 2*(3*8+2)+1
+    (W.TYPE_Q4_0, oracle.ROLE_K, 3, 38, 656),     # quant chunk 2 -> 2^3 = 1: 256 + (24+1)*16
+    (W.TYPE_Q4_0, oracle.ROLE_K, 13, 143, 1967),  # chunk 7 -> 7^5 = 2: 256 + (104+2)*16 + 15
+    (W.TYPE_Q4_0, oracle.ROLE_V, 11, 90, 158),    # block 5 scale: 128 + 16 + 8 + 4 + 2
+    (W.TYPE_Q4_0, oracle.ROLE_V, 6, 1, 49),       # block 0 scale, high byte: 16*3 + 1
+    (W.TYPE_Q4_0, oracle.ROLE_V, 2, 18, 24),      # block 1 scale: 16*1 + 8*1
+    (W.TYPE_Q4_0, oracle.ROLE_V, 9, 1, 7),        # block 0 scale, high byte: 4*1 + 2*1 + 1
+    (W.TYPE_Q8_0, oracle.ROLE_K, 2, 35, 35),      # block 1 scale, high byte: 2*(16+1)+1
+    (W.TYPE_Q8_0, oracle.ROLE_K, 2, 52, 784),     # quant 48 = chunk 3 -> 3^2 = 1: 256 + 33*16
+    (W.TYPE_Q8_0, oracle.ROLE_K, 9, 271, 2799),   # chunk 15 -> 15^1 = 14: 256 + 158*16 + 15
+    (W.TYPE_Q8_0, oracle.ROLE_V, 13, 102, 110),   # block 3 scale: 64 + 16*2 + 8 + 4 + 2
+    (W.TYPE_F16, oracle.ROLE_K, 5, 100, 2612),    # chunk 6 -> 6^5 = 3: (160+3)*16 + 4
+    (W.TYPE_F16, oracle.ROLE_V, 15, 511, 8079),   # chunk 31 -> 31^7 = 24: (480+24)*16 + 15
+]
+
+
+def pin_group_layout():
+    """The oracle's pool layout is the documented one: hand-worked offsets,
+    every byte of a 16-row group written exactly once, and the property the
+    layout exists for -- the eight rows of any 16-byte chunk column fall in
+    eight different 16-byte bank groups (offset / 16 mod 8)."""
+    for t, role, r, i, want in LAYOUT_FIXTURES:
+        assert oracle.group_offset(t, role, r, i) == want, (t, role, r, i)
+    for t in (W.TYPE_F16, W.TYPE_Q4_0, W.TYPE_Q8_0):
+        rb = oracle.row_bytes(t)
+        scales = 0 if t == W.TYPE_F16 else 256
+        for role in (oracle.ROLE_K, oracle.ROLE_V):
+            offs = np.array([[oracle.group_offset(t, role, r, i) for i in range(rb)] for r in range(16)])
+            assert np.array_equal(np.sort(offs.ravel()), np.arange(16 * rb)), (t, role)
+            q = offs[offs >= scales] - scales  # quant region, [16 rows][...]
+            chunk_pos = (q.reshape(16, -1) // 16)
+            for half in (slice(0, 8), slice(8, 16)):
+                banks = chunk_pos[half] % 8
+                for col in range(banks.shape[1]):
+                    assert len(set(banks[:, col])) == 8, (t, role, col)
+    # out-of-range arguments
+    assert oracle.group_offset(W.TYPE_Q4_0, oracle.ROLE_K, 16, 0) == -1
+    assert oracle.group_offset(W.TYPE_Q4_0, 2, 0, 0) == -1
+    assert oracle.group_offset(W.TYPE_Q8_0, oracle.ROLE_V, 0, 272) == -1
+
+
 PINS = [pin_half_all_patterns, pin_q8_0_hand_block, pin_q4_0_hand_block,
         pin_subnormal_and_negative_scales, pin_capacity_table, pin_rdna4_bandwidth,
         pin_quantiser_roundtrip, pin_one_key, pin_identical_keys_and_zero_query, pin_gqa_mapping,
         pin_causal_verify, pin_dominant_key, pin_dense_brute_force,
-        pin_placement_and_page_size_invariance, pin_split_merge, pin_fully_masked_part]
+        pin_placement_and_page_size_invariance, pin_split_merge, pin_fully_masked_part, pin_group_layout]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -376,8 +423,12 @@ MUTATIONS = [
     ("causal_off_by_one", "const long last = L - c->n_qtok + t;", "const long last = L - c->n_qtok + t + 1;"),
     ("no_scale", "z[j - j0] = scale * acc;", "z[j - j0] = acc;"),
     ("slot_off_by_one", "long slot = pos % c->page_size;", "long slot = (pos + 1) % c->page_size;"),
-    ("layout_transposed", "return pool + (((blk * c->hkv + g) * (long)c->page_size + slot) * rb);",
-     "return pool + (((blk * (long)c->page_size + slot) * c->hkv + g) * rb);"),
+    ("layout_transposed",
+     "const uint8_t* grp = pool + ((blk * c->hkv + g) * (long)c->page_size + slot / ORC_GROUP * ORC_GROUP) * rb;",
+     "const uint8_t* grp = pool + ((blk * (long)c->page_size + slot / ORC_GROUP * ORC_GROUP) * c->hkv + g) * rb;"),
+    ("layout_no_swizzle", "return 32L * nb + (r * chunks + (c ^ (r % 8))) * 16 + qi % 16;",
+     "return 32L * nb + (r * chunks + c) * 16 + qi % 16;"),
+    ("v_scale_pairs", "8 * (b % 2) + 4 * (r / 8) + 2 * (r % 2) + o;", "4 * (b % 2) + 8 * (r / 8) + 2 * (r % 2) + o;"),
     ("softmax_sign", "double w = exp(z[j - j0] - m);", "double w = exp(m - z[j - j0]);"),
     ("lse_drops_max", "lse[base] = (l > 0.0) ? m + log(l) : -INFINITY;",
      "lse[base] = (l > 0.0) ? log(l) : -INFINITY;"),
