@@ -61,6 +61,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <type_traits>
 
 #include "pa.h"
 #include "pa_device.cuh"
@@ -319,9 +320,32 @@ __device__ __forceinline__ uint32_t lane_chunk_offset(int lane) {
 
 // ------------------------------------------------------------------ producers
 
-// Table entry of a head-group tile (16 keys: one row group of one page).
-__device__ __forceinline__ int hg_table_entry(const DecodeParams& p, const TilePos& t) {
-  return __ldg(p.table + (long long)t.s * p.table_stride + (t.j * kTileHG) / p.page_size);
+// A head-group tile's place in the CTA's walk, with its page and first slot
+// kept incrementally (no division per tile).
+struct HgPos {
+  TilePos t;
+  int page, slot0;  // page index within the sequence, first slot of the tile in it
+};
+
+__device__ __forceinline__ HgPos hg_start(const DecodeParams& p, const TilePos& t) {
+  const int k0 = t.j * kTileHG;
+  return HgPos{t, k0 / p.page_size, k0 % p.page_size};
+}
+
+__device__ __forceinline__ void hg_next(const DecodeParams& p, HgPos& h) {
+  const int s = h.t.s, g = h.t.g;
+  next_tile(p, h.t);
+  if (h.t.s != s || h.t.g != g) {
+    h.page = 0;
+    h.slot0 = 0;
+  } else if ((h.slot0 += kTileHG) == p.page_size) {
+    h.slot0 = 0;
+    ++h.page;
+  }
+}
+
+__device__ __forceinline__ int hg_table_entry(const DecodeParams& p, const HgPos& h) {
+  return __ldg(p.table + (long long)h.t.s * p.table_stride + h.page);
 }
 
 // Table entry for row group `lane` (0..3) of a per-head tile, -1 past its keys.
@@ -363,17 +387,17 @@ __device__ void produce_hg(const DecodeParams& p, uint32_t ring, uint32_t bar_fu
   int st = 0;
   uint32_t ph = 0;
   long long issued = 0;
-  int tb = hg_table_entry(p, pos), tbn = -1;
+  HgPos cur = hg_start(p, pos);
+  int tb = hg_table_entry(p, cur), tbn = -1;
   for (long long x = a; x < b; ++x) {
     if (*abort) break;
-    TilePos nxt = pos;
+    HgPos nxt = cur;
     if (x + 1 < b) {
-      next_tile(p, nxt);
+      hg_next(p, nxt);
       tbn = hg_table_entry(p, nxt);
     }
     const uint32_t fb = bar_full + 8 * st, eb = bar_empty + 8 * st;
-    if (lane == 0) mbar_wait(eb, ph ^ 1, p.err, abort);
-    __syncwarp();
+    mbar_wait(eb, ph ^ 1, p.err, abort);  // every lane: no divergent branch
     const uint32_t sk = ring + st * G::kBytes, sv = sk + G::kKBytes;
     if (!(tb >= 0 && tb < p.n_blocks)) {
       // Outside the pool: zero rows for every head of the group, no copy.
@@ -385,7 +409,7 @@ __device__ void produce_hg(const DecodeParams& p, uint32_t ring, uint32_t bar_fu
       if (lane == 0) mbar_arrive(fb);
     } else {
       // First row of the group of head h0 = g * GH.
-      const long long row0 = ((long long)tb * H + pos.g * GH) * ps + (pos.j * kTileHG) % ps;
+      const long long row0 = ((long long)tb * H + cur.t.g * GH) * ps + cur.slot0;
       if (whole_blocks) {
         if (lane == 0) {
           mbar_arrive_expect_tx(fb, (uint32_t)H * (G::kKGroup + G::kVGroup));
@@ -405,7 +429,7 @@ __device__ void produce_hg(const DecodeParams& p, uint32_t ring, uint32_t bar_fu
     }
     ++issued;
     if (++st == kStages) { st = 0; ph ^= 1; }
-    pos = nxt;
+    cur = nxt;
     tb = tbn;
   }
   if (lane == 0) drain_ring<kStages>(p, bar_full, abort, st, ph, issued);
@@ -441,8 +465,7 @@ __device__ void produce_head(const DecodeParams& p, uint32_t ring, uint32_t bar_
     const bool mine = lane < ng;
     const bool ok = !mine || (tb >= 0 && tb < p.n_blocks);
     const unsigned bad = __ballot_sync(0xffffffffu, !ok);
-    if (lane == 0) mbar_wait(eb, ph ^ 1, p.err, abort);
-    __syncwarp();
+    mbar_wait(eb, ph ^ 1, p.err, abort);  // every lane: no divergent branch
     const uint32_t sk = ring + st * G::kBytes, sv = sk + G::kKBytes;
     if (bad == 0 && ps % kTile == 0) {
       if (lane == 0) {
@@ -489,17 +512,21 @@ __device__ void produce_head(const DecodeParams& p, uint32_t ring, uint32_t bar_
 // high-half fp16 Q/16) for Q4_0, 1152 * (sum of its fp16 Q) for Q8_0: the
 // magic bias the raw K halves carry, times Q.
 
+// Q fragments are stored two k-steps at a time: entry (k-step pair kp, n-tile
+// nt, lane) is a uint4 {b0, b1 of k-step 2kp, b0, b1 of k-step 2kp+1} at byte
+// ((kp * NT + nt) * 32 + lane) * 16, so one 16-byte load feeds a block's two
+// MMAs.
+
 // Head-group path: warp w stages its own KV head's six query rows (one query
-// token) as S-MMA B fragments ([k-step][lane] uint2) and the block biases
-// ([block][t] float4), from coalesced float4 loads.  Rows 6 and 7 of the
-// fragment (padding) are zero.  Only this warp reads them.
+// token) as S-MMA B fragments and the block biases ([block][t] float4), from
+// coalesced float4 loads.  Rows 6 and 7 of the fragment (padding) are zero.
+// Only this warp reads them.
 template <int KT>
 __device__ void stage_q_warp(const DecodeParams& p, int s, int head, uint32_t qf, float* cb4, int lane) {
   // zero the padding rows 6, 7 (lanes 24..31 of every k-step) and their biases
   if (lane >= 24) {
 #pragma unroll
-    for (int ks = 0; ks < 16; ++ks)
-      asm volatile("st.shared.v2.b32 [%0], {%1, %1};" ::"r"(qf + (ks * 32 + lane) * 8), "r"(0u) : "memory");
+    for (int kp = 0; kp < 8; ++kp) sts128_zero(qf + (kp * 32 + lane) * 16);
   }
   if (KT != PA_F16 && lane < 8) sts128_zero(smem_u32(cb4 + (lane * 4 + 3) * 4));
   const float4* q4 = reinterpret_cast<const float4*>(p.q + ((long long)s * p.n_q_heads + head * kGqa) * kD);
@@ -519,7 +546,7 @@ __device__ void stage_q_warp(const DecodeParams& p, int s, int head, uint32_t qf
       const __half hv = __float2half_rn(sc * vals[k]);
       lo += __half2float(hv);
       const int ln = 4 * row + t;
-      const uint32_t addr = qf + (ks * 32 + ln) * 8 + ((jj >> 3) << 2) + ((jj & 1) << 1);
+      const uint32_t addr = qf + ((ks >> 1) * 32 + ln) * 16 + (ks & 1) * 8 + ((jj >> 3) << 2) + ((jj & 1) << 1);
       asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(__half_as_ushort(hv)) : "memory");
     }
     if (KT != PA_F16) {
@@ -567,9 +594,9 @@ __device__ __forceinline__ float block_bias(const DecodeParams& p, int s, int g,
 }
 
 // Per-head path: stage Q of (sequence s, KV head g) as S-MMA B fragments in
-// the K format's dim order ([k-step][nt][lane] uint2; high-nibble Q4_0
-// k-steps hold Q/16) and, for quantised K, the block biases ([block][nt][t]
-// float4).  All consumer threads take part.
+// the K format's dim order (high-nibble Q4_0 k-steps hold Q/16) and, for
+// quantised K, the block biases ([block][nt][t] float4).  All consumer
+// threads take part.
 template <int KT, int NT>
 __device__ void stage_q(const DecodeParams& p, int s, int g, uint32_t qf, float* cb4, int tid) {
   const int R = kGqa * p.n_qtok;
@@ -584,7 +611,8 @@ __device__ void stage_q(const DecodeParams& p, int s, int g, uint32_t qf, float*
       b0 = pack_half2(f * __ldg(qr + kdim<KT>(ks, 2 * t4)), f * __ldg(qr + kdim<KT>(ks, 2 * t4 + 1)));
       b1 = pack_half2(f * __ldg(qr + kdim<KT>(ks, 2 * t4 + 8)), f * __ldg(qr + kdim<KT>(ks, 2 * t4 + 9)));
     }
-    asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(qf + ((ks * NT + nt) * 32 + ln) * 8), "r"(b0), "r"(b1)
+    asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(qf + (((ks >> 1) * NT + nt) * 32 + ln) * 16 + (ks & 1) * 8),
+                 "r"(b0), "r"(b1)
                  : "memory");
   }
   if (KT != PA_F16) {
@@ -602,20 +630,22 @@ __device__ void stage_q(const DecodeParams& p, int s, int g, uint32_t qf, float*
 // acc[nt] += S^T for the 16 keys of one K row group (rows = keys g, g+8)
 // against the staged Q fragments, over all 256 dims.  kq: this lane's
 // ldmatrix address in the group's chunk region (lane_chunk_offset); ksc: the
-// group's scale region; qf: this lane's Q fragments; cbl: this lane's block
-// bias entries (t = lane & 3).
+// group's scale region; qf: this lane's Q fragments (base + 16 * lane); cbl:
+// this lane's block bias entries (t = lane & 3).
 template <int KT, int NT>
 __device__ __forceinline__ void s_phase(float (&acc)[NT][4], uint32_t kq, uint32_t ksc, uint32_t qf, uint32_t cbl,
                                         int lane) {
   if constexpr (KT == PA_F16) {
 #pragma unroll
-    for (int s = 0; s < 16; ++s) {
-      uint32_t a[4];
-      ldsm_x4(kq ^ ((2 * s) << 4), a);
+    for (int kp = 0; kp < 8; ++kp) {
+      uint32_t a0[4], a1[4];
+      ldsm_x4(kq ^ ((4 * kp) << 4), a0);
+      ldsm_x4(kq ^ ((4 * kp + 2) << 4), a1);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        const uint2 q = lds64(qf + (s * NT + nt) * 256);
-        mma_16816(acc[nt], a, q.x, q.y);
+        const uint4 q = lds128(qf + (kp * NT + nt) * 512);
+        mma_16816(acc[nt], a0, q.x, q.y);
+        mma_16816(acc[nt], a1, q.z, q.w);
       }
     }
   } else {
@@ -661,9 +691,9 @@ __device__ __forceinline__ void s_phase(float (&acc)[NT][4], uint32_t kq, uint32
         for (int nt = 0; nt < NT; ++nt) {
           const float4 c = lds128f(cbl + (b * NT + nt) * 64);
           float tmp[4] = {c.x, c.y, c.z, c.w};
-          const uint2 q0 = lds64(qf + ((2 * b) * NT + nt) * 256), q1 = lds64(qf + ((2 * b + 1) * NT + nt) * 256);
-          mma_16816(tmp, a0, q0.x, q0.y);
-          mma_16816(tmp, a1, q1.x, q1.y);
+          const uint4 q = lds128(qf + (b * NT + nt) * 512);
+          mma_16816(tmp, a0, q.x, q.y);
+          mma_16816(tmp, a1, q.z, q.w);
           acc[nt][0] = fmaf(d0, tmp[0], acc[nt][0]);
           acc[nt][1] = fmaf(d0, tmp[1], acc[nt][1]);
           acc[nt][2] = fmaf(d1, tmp[2], acc[nt][2]);
@@ -863,6 +893,7 @@ __device__ __forceinline__ void write_row_stats(const DecodeParams& p, bool whol
 // ------------------------------------------------------------------ head-group consumer
 
 // One query token: warp w owns KV head (group * GH + w); see the file comment.
+// Only warps w < GH run this (the empty barriers count GH arrivals).
 template <int KT, int VT>
 __device__ void consume_hg(const DecodeParams& p, uint8_t* smem, uint32_t ring, uint32_t bar_full,
                            uint32_t bar_empty, volatile int* abort, long long a, long long b, int s, int g, int j) {
@@ -873,13 +904,13 @@ __device__ void consume_hg(const DecodeParams& p, uint8_t* smem, uint32_t ring, 
   const int gq = lane >> 2, tq = lane & 3;
   const uint32_t qf = ring + SM::kWQ + warp * SM::kWQBytes;
   float* cb4 = reinterpret_cast<float*>(smem + SM::kWCb + warp * SM::kWCbBytes);
-  const uint32_t qf_lane = qf + lane * 8;
+  const uint32_t qf_lane = qf + lane * 16;
   const uint32_t cb_lane = smem_u32(cb4) + 16 * tq;
   // This warp's K and V row groups in stage 0, and its lanes' fragment addresses.
   const uint32_t kg0 = ring + warp * G::kKGroup, vg0 = ring + G::kKBytes + warp * G::kVGroup;
   const uint32_t kq0 = kg0 + Fmt<KT>::kScales + lane_chunk_offset<KT>(lane);
   const uint32_t vq0 = vg0 + Fmt<VT>::kScales + lane_chunk_offset<VT>(lane);
-  const bool active = warp < p.seg_heads;
+  const float scale_log2 = p.scale_log2;
   int st = 0;
   uint32_t ph = 0;
   long long x = a;
@@ -890,7 +921,7 @@ __device__ void consume_hg(const DecodeParams& p, uint8_t* smem, uint32_t ring, 
     const int seg = s * p.segs_per_seq + g;
     const bool whole = (jb == 0 && je == ntl);
     const int head = g * p.seg_heads + warp;
-    if (active) stage_q_warp<KT>(p, s, head, qf, cb4, lane);
+    stage_q_warp<KT>(p, s, head, qf, cb4, lane);
 
     float o[16][4];
 #pragma unroll
@@ -900,95 +931,95 @@ __device__ void consume_hg(const DecodeParams& p, uint8_t* smem, uint32_t ring, 
     float mref0 = -INFINITY, mref1 = -INFINITY;  // rows 2tq, 2tq+1
     float ls0 = 0.f, ls1 = 0.f;                  // this thread's share of the row sums
 
-    const int vis = L - 1;  // last visible key (one query token)
-    for (int jt = jb; jt < je; ++jt) {
-      if (!*abort) mbar_wait(bar_full + 8 * st, ph, p.err, abort);
-      if (active) {
-        const uint32_t so = st * SM::kStageBytes;
-        const int k0 = jt * kTileHG;
-        const bool need_mask = (k0 + kTileHG - 1) > vis;
-        if (need_mask) zero_tail_group<VT>(vg0 + so, vis + 1 - k0, lane);
-        float sacc[1][4] = {{0.f, 0.f, 0.f, 0.f}};
-        s_phase<KT, 1>(sacc, kq0 + so, kg0 + so, qf_lane, cb_lane, lane);
-        float xv[4];
+    // One tile; kMask: the sequence's partial last tile (keys >= L masked).
+    auto tile = [&](auto mask_tag, int jt) {
+      constexpr bool kMask = decltype(mask_tag)::value;
+      mbar_wait(bar_full + 8 * st, ph, p.err, abort);
+      const uint32_t so = st * SM::kStageBytes;
+      const int n = L - jt * kTileHG;  // keys of this tile that exist (< 16 only when masked)
+      if (kMask) zero_tail_group<VT>(vg0 + so, n, lane);
+      float sacc[1][4] = {{0.f, 0.f, 0.f, 0.f}};
+      s_phase<KT, 1>(sacc, kq0 + so, kg0 + so, qf_lane, cb_lane, lane);
+      float xv[4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          xv[c] = sacc[0][c] * p.scale_log2;
-          if (need_mask && k0 + gq + ((c & 2) ? 8 : 0) > vis) xv[c] = -INFINITY;
-        }
-        // ---- lazy running max
-        const bool up = (xv[0] > mref0 + kLazy) || (xv[2] > mref0 + kLazy) || (xv[1] > mref1 + kLazy) ||
-                        (xv[3] > mref1 + kLazy);
-        if (__any_sync(0xffffffffu, up)) {
-          float mx0 = fmaxf(xv[0], xv[2]), mx1 = fmaxf(xv[1], xv[3]);
-#pragma unroll
-          for (int off = 4; off < 32; off <<= 1) {
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-          }
-          const float mn0 = fmaxf(mref0, mx0), mn1 = fmaxf(mref1, mx1);
-          const float al0 = (mn0 == -INFINITY) ? 1.f : exp2f(mref0 - mn0);
-          const float al1 = (mn1 == -INFINITY) ? 1.f : exp2f(mref1 - mn1);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            o[i][0] *= al0; o[i][2] *= al0;
-            o[i][1] *= al1; o[i][3] *= al1;
-          }
-          ls0 *= al0;
-          ls1 *= al1;
-          mref0 = mn0;
-          mref1 = mn1;
-        }
-        const float b0 = (mref0 == -INFINITY) ? 0.f : mref0, b1 = (mref1 == -INFINITY) ? 0.f : mref1;
-        const uint32_t X0 = pack_half2(exp2f(xv[0] - b0), exp2f(xv[1] - b1));  // key gq: rows 2tq, 2tq+1
-        const uint32_t X1 = pack_half2(exp2f(xv[2] - b0), exp2f(xv[3] - b1));  // key gq+8
-        {
-          const float2 f0 = half2_bits_to_float2(X0), f1 = half2_bits_to_float2(X1);
-          ls0 += f0.x + f1.x;
-          ls1 += f0.y + f1.y;
-        }
-        const uint32_t B0 = movmatrix_trans(X0), B1 = movmatrix_trans(X1);
-        pv_solo<VT>(o, vq0 + so, vg0 + so, lane, B0, B1);
+      for (int c = 0; c < 4; ++c) {
+        xv[c] = sacc[0][c] * scale_log2;
+        if (kMask && gq + ((c & 2) ? 8 : 0) >= n) xv[c] = -INFINITY;
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_empty + 8 * st);
-      if (++st == kStages) { st = 0; ph ^= 1; }
-    }
-
-    // ---- piece result for this warp's head: rows 2tq, 2tq+1 (< 6)
-    if (active) {
+      // ---- lazy running max
+      const bool up = (xv[0] > mref0 + kLazy) || (xv[2] > mref0 + kLazy) || (xv[1] > mref1 + kLazy) ||
+                      (xv[3] > mref1 + kLazy);
+      if (__any_sync(0xffffffffu, up)) {
+        float mx0 = fmaxf(xv[0], xv[2]), mx1 = fmaxf(xv[1], xv[3]);
 #pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        ls0 += __shfl_xor_sync(0xffffffffu, ls0, off);
-        ls1 += __shfl_xor_sync(0xffffffffu, ls1, off);
-      }
-      const int slot = (int)blockIdx.x + seg;
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const int hl = 2 * tq + c;
-        if (hl >= kGqa) continue;
-        const float lr = c ? ls1 : ls0, mr = c ? mref1 : mref0;
-        const int row = warp * kGqa + hl;  // row within the segment
-        float* dst;
-        float inv = 1.f;
-        if (whole) {
-          dst = p.out + ((long long)s * p.n_q_heads + head * kGqa + hl) * kD;
-          inv = lr > 0.f ? 1.f / lr : 0.f;
-        } else {
-          dst = p.part_o + ((long long)slot * p.rows_per_seg + row) * kD;
+        for (int off = 4; off < 32; off <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
         }
+        const float mn0 = fmaxf(mref0, mx0), mn1 = fmaxf(mref1, mx1);
+        const float al0 = (mn0 == -INFINITY) ? 1.f : ex2(mref0 - mn0);
+        const float al1 = (mn1 == -INFINITY) ? 1.f : ex2(mref1 - mn1);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          dst[vdim<VT>(gq, i, 0)] = o[i][c] * inv;
-          dst[vdim<VT>(gq, i, 1)] = o[i][2 + c] * inv;
+          o[i][0] *= al0; o[i][2] *= al0;
+          o[i][1] *= al1; o[i][3] *= al1;
         }
-        if (gq == 0) {
-          if (whole) {
-            if (p.lse)
-              p.lse[(long long)s * p.n_q_heads + head * kGqa + hl] = lr > 0.f ? (mr + log2f(lr)) * kLn2 : -INFINITY;
-          } else {
-            p.part_ml[(long long)slot * p.rows_per_seg + row] = make_float2(mr, lr);
-          }
+        ls0 *= al0;
+        ls1 *= al1;
+        mref0 = mn0;
+        mref1 = mn1;
+      }
+      const float b0 = (mref0 == -INFINITY) ? 0.f : mref0, b1 = (mref1 == -INFINITY) ? 0.f : mref1;
+      const uint32_t X0 = pack_half2(ex2(xv[0] - b0), ex2(xv[1] - b1));  // key gq: rows 2tq, 2tq+1
+      const uint32_t X1 = pack_half2(ex2(xv[2] - b0), ex2(xv[3] - b1));  // key gq+8
+      {
+        const float2 f0 = half2_bits_to_float2(X0), f1 = half2_bits_to_float2(X1);
+        ls0 += f0.x + f1.x;
+        ls1 += f0.y + f1.y;
+      }
+      const uint32_t B0 = movmatrix_trans(X0), B1 = movmatrix_trans(X1);
+      pv_solo<VT>(o, vq0 + so, vg0 + so, lane, B0, B1);
+      __syncwarp();
+      mbar_arrive_warp(bar_empty + 8 * st);
+      if (++st == kStages) { st = 0; ph ^= 1; }
+    };
+    // Every tile but a partial last one runs unmasked.
+    const int je_full = (je == ntl && (L % kTileHG) != 0) ? je - 1 : je;
+    for (int jt = jb; jt < je_full; ++jt) tile(std::false_type{}, jt);
+    if (je_full < je) tile(std::true_type{}, je_full);
+
+    // ---- piece result for this warp's head: rows 2tq, 2tq+1 (< 6)
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      ls0 += __shfl_xor_sync(0xffffffffu, ls0, off);
+      ls1 += __shfl_xor_sync(0xffffffffu, ls1, off);
+    }
+    const int slot = (int)blockIdx.x + seg;
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const int hl = 2 * tq + c;
+      if (hl >= kGqa) continue;
+      const float lr = c ? ls1 : ls0, mr = c ? mref1 : mref0;
+      const int row = warp * kGqa + hl;  // row within the segment
+      float* dst;
+      float inv = 1.f;
+      if (whole) {
+        dst = p.out + ((long long)s * p.n_q_heads + head * kGqa + hl) * kD;
+        inv = lr > 0.f ? 1.f / lr : 0.f;
+      } else {
+        dst = p.part_o + ((long long)slot * p.rows_per_seg + row) * kD;
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        dst[vdim<VT>(gq, i, 0)] = o[i][c] * inv;
+        dst[vdim<VT>(gq, i, 1)] = o[i][2 + c] * inv;
+      }
+      if (gq == 0) {
+        if (whole) {
+          if (p.lse)
+            p.lse[(long long)s * p.n_q_heads + head * kGqa + hl] = lr > 0.f ? (mr + log2f(lr)) * kLn2 : -INFINITY;
+        } else {
+          p.part_ml[(long long)slot * p.rows_per_seg + row] = make_float2(mr, lr);
         }
       }
     }
@@ -1033,7 +1064,7 @@ __device__ void consume_shared(const DecodeParams& p, uint8_t* smem, uint32_t ri
     float* cb4 = reinterpret_cast<float*>(smem + SM::kCb + qbuf * SM::kCbBuf);
     stage_q<KT, NT>(p, s, g, qf, cb4, tid);
     named_bar_sync(1, kCWarps * 32);
-    const uint32_t qf_lane = qf + lane * 8;
+    const uint32_t qf_lane = qf + lane * 16;
     const uint32_t cb_lane = smem_u32(cb4) + 16 * tq;
 
     float o[4][NT][4];
@@ -1050,7 +1081,7 @@ __device__ void consume_shared(const DecodeParams& p, uint8_t* smem, uint32_t ri
     const int vis0 = L - p.n_qtok;  // last key visible to query token 0
     for (int jt = jb; jt < je; ++jt) {
       const uint32_t fb = bar_full + 8 * st;
-      if (!*abort) mbar_wait(fb, ph, p.err, abort);
+      mbar_wait(fb, ph, p.err, abort);
       const uint32_t so = st * SM::kStageBytes;
       const int k0 = jt * kTile;
       if (k0 + kTile > L) zero_tail_tile<VT>(vs0 + so, L - k0, warp, lane);
@@ -1153,7 +1184,7 @@ __device__ void consume_shared(const DecodeParams& p, uint8_t* smem, uint32_t ri
         pv_kstep<VT, NT>(o, vg + vq_off, vg, warp, lane, bp);
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_empty + 8 * st);
+      mbar_arrive_warp(bar_empty + 8 * st);
       if (++st == kStages) { st = 0; ph ^= 1; }
       tbuf ^= 1;
     }
@@ -1221,7 +1252,7 @@ __global__ void __launch_bounds__(kThreads, CtaTarget<KT, VT, NT>::kN)
     *abort = 0;
     for (int i = 0; i < kStages; ++i) {
       mbar_init(bar_full + 8 * i, 1);
-      mbar_init(bar_empty + 8 * i, kCWarps);
+      mbar_init(bar_empty + 8 * i, NT == 1 ? p.seg_heads : kCWarps);  // one arrival per consuming warp
     }
     fence_mbar_init();
     int s0, g0, j0;
@@ -1248,6 +1279,7 @@ __global__ void __launch_bounds__(kThreads, CtaTarget<KT, VT, NT>::kN)
     return;
   }
   if constexpr (NT == 1) {
+    if (warp >= p.seg_heads) return;  // a head group smaller than the warp count
     consume_hg<KT, VT>(p, smem, ring, bar_full, bar_empty, abort, a, b, s, g, j);
   } else {
     consume_shared<KT, VT, NT>(p, smem, ring, bar_full, bar_empty, abort, a, b, s, g, j);

@@ -63,16 +63,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait for the phase with the given parity.  Returns false (after
-// recording PA_ERR_TIMEOUT and raising *abort) if the phase did not complete
-// within the time limit, or at once if *abort is already raised and
-// `honour_abort` is set.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t* err, volatile int* abort,
-                                          bool honour_abort = true, uint64_t limit_ns = kWaitTimeoutNs) {
-  if (mbar_try_wait(bar, parity)) return true;
+// try_wait that may suspend the thread for up to hint_ns while the phase is
+// incomplete (it returns early when the phase completes).
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Out-of-line part of mbar_wait: poll with a suspend hint, check the abort
+// flag every 16 polls and give up after limit_ns of wall time.
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, int32_t* err,
+                                                   volatile int* abort, bool honour_abort, uint64_t limit_ns) {
   const uint64_t t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_hint(bar, parity, 20000u)) return true;
     if ((i & 15u) == 0) {
       if (honour_abort && abort && *abort) return false;
       if (globaltimer() - t0 > limit_ns) {
@@ -82,6 +91,24 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t
       }
     }
   }
+}
+
+// Bounded wait for the phase with the given parity.  Returns false (after
+// recording PA_ERR_TIMEOUT and raising *abort) if the phase did not complete
+// within the time limit, or once *abort is seen raised while waiting and
+// `honour_abort` is set.  A phase already complete costs one try_wait.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t* err, volatile int* abort,
+                                          bool honour_abort = true, uint64_t limit_ns = kWaitTimeoutNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, err, abort, honour_abort, limit_ns);
+}
+
+// One arrival for the whole (converged) warp, made by an elected lane.
+__device__ __forceinline__ void mbar_arrive_warp(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\t@P mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}" ::"r"(
+          bar)
+      : "memory");
 }
 
 // ---------------------------------------------------------------- bulk copy
@@ -237,6 +264,14 @@ __device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4],
       "{%0,%1,%2,%3};\n"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// 2^x (hardware approximation, relative error about 2^-22; flushes results
+// below 2^-126 to 0).  Used for softmax weights that are rounded to fp16.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // Transpose an 8x8 matrix of 16-bit elements held one row-pair per thread.
