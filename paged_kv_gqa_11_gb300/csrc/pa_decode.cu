@@ -3,11 +3,12 @@
 // pa_decode_impl.cuh and is instantiated once per K format in
 // pa_decode_kern_*.cu.
 //
-// Planning ("occupancy-aware context parallelism", lucebox PR #555, Summary):
-// the batch's 64-key tiles, counted from the host copy of the sequence
+// Planning (lucebox PR #555, Summary: context parallelism sized by
+// occupancy): the batch's tiles, counted from the host copy of the sequence
 // lengths, are cut into as many equal contiguous ranges as CTAs of the chosen
 // kernel fit on the device at once (occupancy x SM count, at most one range
-// per tile).  The merge kernel follows as a programmatic dependent launch.
+// per tile).  The host also lists the merge tasks; the merge kernel follows
+// as a programmatic dependent launch.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -33,231 +34,177 @@ namespace {
 //
 // Two levels in one launch, so a segment cut into hundreds of pieces (a long
 // sequence spread over the whole GPU) still merges with every SM pulling data.
-// The grid holds exactly one CTA per (task, row), a task being a chunk of up
-// to 32 pieces of a segment that has more than one piece; each CTA finds its
-// task with a block scan over the sequence lengths.  Level 1: each of the 8
-// warps loads its 4 pieces at once and folds them with the chunk maximum.  A
-// segment with one chunk writes its result directly; otherwise each chunk
-// stores (M, W, O) at its first piece's slot and the last chunk to arrive (a
-// counter the split kernel zeroed) merges the chunk results in chunk order,
-// so the result does not depend on timing.  Launched as a programmatic
-// dependent of the split kernel.
+// A task is a chunk of up to 32 consecutive pieces of one multi-piece segment;
+// the host lists the tasks in the launch parameters and the grid holds one CTA
+// per (task, row).  Level 1: warp w loads its four pieces (partial and (m, l))
+// in one go and folds them against its own maximum; one barrier later 64
+// threads fold the eight warps, a float4 of dims each.  A segment with one
+// chunk writes its result directly; otherwise each chunk stores (M, W, O) at
+// its first piece's slot and the last chunk to arrive (a counter the split
+// kernel zeroed) folds the chunk results in chunk order, so the result does
+// not depend on timing.  Launched as a programmatic dependent of the split
+// kernel: the task decode runs before griddepcontrol.wait.
 constexpr int kMergeThreads = 256;
 constexpr int kMergeWarps = kMergeThreads / 32;
-constexpr int kChunk = 32;                          // pieces per task
-constexpr int kPerWarp = kChunk / kMergeWarps;      // pieces per warp
+constexpr int kChunk = 32;                      // pieces per task
+constexpr int kPerWarp = kChunk / kMergeWarps;  // pieces per warp
+constexpr int kMaxTasks = 1024;                 // bounded by about 1.04 x the split grid
 
-// Exclusive block-wide prefix sum of one int per thread; *total gets the sum.
-__device__ __forceinline__ int block_exclusive_scan(int v, int* sh, int* total) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  __syncthreads();
-  if (lane == 31) sh[warp] = x;
-  __syncthreads();
-  int before = 0, all = 0;
-  for (int i = 0; i < kMergeWarps; ++i) {
-    if (i < warp) before += sh[i];
-    all += sh[i];
-  }
-  *total = all;
-  return before + x - v;
+// Task word: c0 (first CTA holding a piece of the segment) << 17 | chunk << 11 | pieces.
+struct MergeParams {
+  DecodeParams p;
+  int2 task[kMaxTasks];  // {segment, packed word}
+};
+
+__device__ __forceinline__ float4 f4_fma(float f, float4 x, float4 acc) {
+  return make_float4(fmaf(f, x.x, acc.x), fmaf(f, x.y, acc.y), fmaf(f, x.z, acc.z), fmaf(f, x.w, acc.w));
 }
 
-__device__ __forceinline__ int pieces_of(long long seg_start, int ntl, const DecodeParams& p, int* c0) {
-  *c0 = cta_of_tile(seg_start, p.total_tiles, p.n_ctas);
-  return cta_of_tile(seg_start + ntl - 1, p.total_tiles, p.n_ctas) - *c0 + 1;
-}
-
-// Fold per-warp states (m, W, O relative to m) into one: warp 0 finds the
-// maximum and the scale of every warp; 64 threads add the float4 columns.
-// Result: O (relative to M) in part[0], returns (M, W).
-__device__ __forceinline__ float2 fold_warps(float m, float w, float4 a0, float4 a1, float* wm, float* ww,
-                                             float* wf, float4 (*part)[kD / 4]) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  part[warp][2 * lane] = a0;
-  part[warp][2 * lane + 1] = a1;
-  if (lane == 0) { wm[warp] = m; ww[warp] = w; }
-  __syncthreads();
-  if (warp == 0) {
-    const float mi = lane < kMergeWarps ? wm[lane] : -INFINITY;
-    const float wi = lane < kMergeWarps ? ww[lane] : 0.f;
-    float M = (wi > 0.f) ? mi : -INFINITY;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    const float f = (M == -INFINITY || !(wi > 0.f)) ? 0.f : exp2f(mi - M);
-    float W = f * wi;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
-    if (lane < kMergeWarps) wf[lane] = f;
-    if (lane == 0) { wm[kMergeWarps] = M; ww[kMergeWarps] = W; }
-  }
-  __syncthreads();
-  if (tid < kD / 4) {
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int i = 0; i < kMergeWarps; ++i) {
-      const float f = wf[i];
-      const float4 u = part[i][tid];
-      o.x += f * u.x; o.y += f * u.y; o.z += f * u.z; o.w += f * u.w;
-    }
-    part[0][tid] = o;  // thread tid is the only reader and writer of entry tid here
-  }
-  __syncthreads();
-  return make_float2(wm[kMergeWarps], ww[kMergeWarps]);
-}
-
-__global__ void __launch_bounds__(kMergeThreads) pa_merge_kernel(const __grid_constant__ DecodeParams p) {
-  __shared__ int sh[kMergeWarps];
-  __shared__ int found[4];
-  __shared__ float wm[kMergeWarps + 1], ww[kMergeWarps + 1], wf[kMergeWarps];
+__global__ void __launch_bounds__(kMergeThreads) pa_merge_kernel(const __grid_constant__ MergeParams mp) {
+  const DecodeParams& p = mp.p;
+  __shared__ float wm[kMergeWarps], ww[kMergeWarps];
   __shared__ float4 part[kMergeWarps][kD / 4];
   __shared__ int is_last;
-  const int task = blockIdx.x, row = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-
-  // ---- find this CTA's (segment, chunk): scan sequences in batches
-  if (tid == 0) found[0] = -1;
-  long long tiles_carry = 0;
-  int task_carry = 0;
-  for (int base = 0; base < p.n_seq; base += kMergeThreads) {
-    const int s = base + tid;
-    const int ntl = s < p.n_seq ? tiles_of(p, p.seq_lens[s]) : 0;
-    int tile_total;
-    const long long tb = tiles_carry + block_exclusive_scan(ntl, sh, &tile_total);
-    int my_tasks = 0;
-    for (int g = 0; s < p.n_seq && g < p.segs_per_seq; ++g) {
-      int c0;
-      const int np = pieces_of(tb * p.segs_per_seq + (long long)g * ntl, ntl, p, &c0);
-      if (np > 1) my_tasks += (np + kChunk - 1) / kChunk;
-    }
-    int task_total;
-    const int t0 = task_carry + block_exclusive_scan(my_tasks, sh, &task_total);
-    if (task >= t0 && task < t0 + my_tasks) {  // exactly one thread
-      int t = t0;
-      for (int g = 0; g < p.segs_per_seq; ++g) {
-        int c0;
-        const int np = pieces_of(tb * p.segs_per_seq + (long long)g * ntl, ntl, p, &c0);
-        const int nc = np > 1 ? (np + kChunk - 1) / kChunk : 0;
-        if (task < t + nc) {
-          found[0] = s * p.segs_per_seq + g;
-          found[1] = task - t;
-          found[2] = c0;
-          found[3] = np;
-          break;
-        }
-        t += nc;
-      }
-    }
-    __syncthreads();
-    if (found[0] >= 0) break;
-    tiles_carry += tile_total;
-    task_carry += task_total;
-  }
-  // Every CTA waits for the split grid before it exits, so the merge grid
-  // completing implies the split grid completed (stream order for later work).
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int seg = found[0];
-  if (seg < 0) return;
-  const int chunk = found[1], c0 = found[2], np = found[3];
+  const int row = blockIdx.y, R = p.rows_per_seg;
+  const int2 tk = mp.task[blockIdx.x];
+  const int seg = tk.x, c0 = tk.y >> 17, chunk = (tk.y >> 11) & 63, np = tk.y & 2047;
   const int n_chunks = (np + kChunk - 1) / kChunk;
+  const int cbeg = c0 + kChunk * chunk, cend = min(c0 + np, cbeg + kChunk);  // pieces [cbeg, cend)
   const int s = seg / p.segs_per_seq, g = seg % p.segs_per_seq;
-  const int R = p.rows_per_seg;
-
-  // ---- level 1: pieces c0 + 32 chunk + 4 warp + k
-  const int cbeg = c0 + kChunk * chunk, cend = min(c0 + np, cbeg + kChunk);  // [cbeg, cend)
-  float cm = -INFINITY;  // chunk maximum (over pieces with weight)
-  if (warp == 0) {
-    float v = -INFINITY;
-    if (cbeg + lane < cend) {
-      const float2 ml = __ldcg(p.part_ml + (long long)(cbeg + lane + seg) * R + row);
-      if (ml.y > 0.f) v = ml.x;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    if (lane == 0) wm[kMergeWarps] = v;
-  }
-  __syncthreads();
-  cm = wm[kMergeWarps];
-  float2 mlv[kPerWarp];
-  float4 x0[kPerWarp], x1[kPerWarp];
-#pragma unroll
-  for (int k = 0; k < kPerWarp; ++k) {
-    const int c = cbeg + kPerWarp * warp + k;
-    mlv[k] = make_float2(-INFINITY, 0.f);
-    x0[k] = x1[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (c < cend) {
-      const long long slot = (long long)(c + seg) * R + row;
-      mlv[k] = __ldcg(p.part_ml + slot);
-      const float4* src = reinterpret_cast<const float4*>(p.part_o + slot * kD);
-      x0[k] = __ldcg(src + 2 * lane);
-      x1[k] = __ldcg(src + 2 * lane + 1);
-    }
-  }
-  float wsum = 0.f;
-  float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
-#pragma unroll
-  for (int k = 0; k < kPerWarp; ++k) {
-    const float wt = (mlv[k].y > 0.f && cm != -INFINITY) ? exp2f(mlv[k].x - cm) : 0.f;
-    wsum += wt * mlv[k].y;
-    a0.x += wt * x0[k].x; a0.y += wt * x0[k].y; a0.z += wt * x0[k].z; a0.w += wt * x0[k].w;
-    a1.x += wt * x1[k].x; a1.y += wt * x1[k].y; a1.z += wt * x1[k].z; a1.w += wt * x1[k].w;
-  }
-  float2 MW = fold_warps(cm, wsum, a0, a1, wm, ww, wf, part);
-
-  if (n_chunks > 1) {
-    const long long mslot = (long long)(cbeg + seg) * R + row;
-    if (tid < kD / 4) reinterpret_cast<float4*>(p.mid_o + mslot * kD)[tid] = part[0][tid];
-    if (tid == 0) p.mid_ml[mslot] = MW;
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) is_last = atomicAdd(p.merge_count + (long long)seg * R + row, 1) == n_chunks - 1;
-    __syncthreads();
-    if (!is_last) return;
-    __threadfence();
-    // ---- level 2: chunk results; warp w folds chunks w, w+8, ... in order
-    float m = -INFINITY, w = 0.f;
-    a0 = make_float4(0.f, 0.f, 0.f, 0.f);
-    a1 = a0;
-    for (int k = warp; k < n_chunks; k += kMergeWarps) {
-      const long long ms = (long long)(c0 + kChunk * k + seg) * R + row;
-      const float2 v = __ldcg(p.mid_ml + ms);
-      const float4* src = reinterpret_cast<const float4*>(p.mid_o + ms * kD);
-      const float4 y0 = __ldcg(src + 2 * lane), y1 = __ldcg(src + 2 * lane + 1);
-      if (!(v.y > 0.f)) continue;
-      const float mn = fmaxf(m, v.x);
-      const float sa = (m == -INFINITY) ? 0.f : exp2f(m - mn), sb = exp2f(v.x - mn);
-      a0.x = a0.x * sa + y0.x * sb; a0.y = a0.y * sa + y0.y * sb;
-      a0.z = a0.z * sa + y0.z * sb; a0.w = a0.w * sa + y0.w * sb;
-      a1.x = a1.x * sa + y1.x * sb; a1.y = a1.y * sa + y1.y * sb;
-      a1.z = a1.z * sa + y1.z * sb; a1.w = a1.w * sa + y1.w * sb;
-      w = w * sa + v.y * sb;
-      m = mn;
-    }
-    MW = fold_warps(m, w, a0, a1, wm, ww, wf, part);
-    if (tid == 0) p.merge_count[(long long)seg * R + row] = 0;
-  }
-
   // Segment row -> output row: a head group's rows are (head, query head) of
   // one token; a single head's rows are (token, query head).
   long long orow;
   if (p.seg_heads > 1 || p.n_qtok == 1) {
     orow = (long long)s * p.n_q_heads + (long long)g * p.seg_heads * kGqa + row;
   } else {
-    const int tk = row / kGqa, hl = row % kGqa;
-    orow = ((long long)s * p.n_qtok + tk) * p.n_q_heads + g * kGqa + hl;
+    const int t = row / kGqa, hl = row % kGqa;
+    orow = ((long long)s * p.n_qtok + t) * p.n_q_heads + g * kGqa + hl;
   }
-  const float inv = MW.y > 0.f ? 1.f / MW.y : 0.f;
+  // Every CTA waits for the split grid before it reads a partial (and before
+  // it exits, so the merge grid completing implies the split grid completed).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  // ---- level 1: warp w folds pieces cbeg + 4w + k against its own maximum
+  float2 ml[kPerWarp];
+  float4 x0[kPerWarp], x1[kPerWarp];
+#pragma unroll
+  for (int k = 0; k < kPerWarp; ++k) {
+    const int c = cbeg + kPerWarp * warp + k;
+    ml[k] = make_float2(-INFINITY, 0.f);
+    x0[k] = x1[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (c < cend) {
+      const long long slot = (long long)(c + seg) * R + row;
+      ml[k] = __ldcg(p.part_ml + slot);
+      const float4* src = reinterpret_cast<const float4*>(p.part_o + slot * kD);
+      x0[k] = __ldcg(src + 2 * lane);
+      x1[k] = __ldcg(src + 2 * lane + 1);
+    }
+  }
+  float mw = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < kPerWarp; ++k)
+    if (ml[k].y > 0.f) mw = fmaxf(mw, ml[k].x);
+  float wsum = 0.f;
+  float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+#pragma unroll
+  for (int k = 0; k < kPerWarp; ++k) {
+    const float f = (ml[k].y > 0.f) ? exp2f(ml[k].x - mw) : 0.f;
+    wsum = fmaf(f, ml[k].y, wsum);
+    a0 = f4_fma(f, x0[k], a0);
+    a1 = f4_fma(f, x1[k], a1);
+  }
+  part[warp][2 * lane] = a0;
+  part[warp][2 * lane + 1] = a1;
+  if (lane == 0) { wm[warp] = mw; ww[warp] = wsum; }
+  __syncthreads();
+  // Fold the warps (64 threads, one float4 of dims each).
+  float M = -INFINITY, W = 0.f;
+  float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
   if (tid < kD / 4) {
-    float4 o = part[0][tid];
-    o.x *= inv; o.y *= inv; o.z *= inv; o.w *= inv;
-    reinterpret_cast<float4*>(p.out + orow * kD)[tid] = o;
+#pragma unroll
+    for (int i = 0; i < kMergeWarps; ++i)
+      if (ww[i] > 0.f) M = fmaxf(M, wm[i]);
+#pragma unroll
+    for (int i = 0; i < kMergeWarps; ++i) {
+      const float f = (ww[i] > 0.f) ? exp2f(wm[i] - M) : 0.f;
+      W = fmaf(f, ww[i], W);
+      O = f4_fma(f, part[i][tid], O);
+    }
   }
-  if (tid == 0 && p.lse) p.lse[orow] = MW.y > 0.f ? (MW.x + log2f(MW.y)) * kLn2 : -INFINITY;
+
+  if (n_chunks > 1) {
+    const long long mslot = (long long)(cbeg + seg) * R + row;
+    if (tid < kD / 4) reinterpret_cast<float4*>(p.mid_o + mslot * kD)[tid] = O;
+    if (tid == 0) p.mid_ml[mslot] = make_float2(M, W);
+    __syncthreads();
+    if (tid == 0) {
+      __threadfence();  // cumulative: publishes the CTA's stores ordered before it by the barrier
+      is_last = atomicAdd(p.merge_count + (long long)seg * R + row, 1) == n_chunks - 1;
+    }
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+    // ---- level 2: the chunk results, in chunk order.  Quarter q (64 threads,
+    // a float4 of dims each) folds chunks q, q + 4, ... with every load in
+    // flight at once, then 64 threads fold the quarters.
+    const int q = tid >> 6, d4 = tid & 63;
+    constexpr int kPerQ = 4;  // chunks per quarter per round (16 per round)
+    float mq = -INFINITY, wq = 0.f;
+    float4 oq = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int base = 0; base < n_chunks; base += 4 * kPerQ) {
+      float2 cm[kPerQ];
+      float4 cy[kPerQ];
+#pragma unroll
+      for (int i = 0; i < kPerQ; ++i) {
+        const int k = base + q + 4 * i;
+        cm[i] = make_float2(-INFINITY, 0.f);
+        cy[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (k < n_chunks) {
+          const long long ms = (long long)(c0 + kChunk * k + seg) * R + row;
+          cm[i] = __ldcg(p.mid_ml + ms);
+          cy[i] = __ldcg(reinterpret_cast<const float4*>(p.mid_o + ms * kD) + d4);
+        }
+      }
+      float mr = mq;
+#pragma unroll
+      for (int i = 0; i < kPerQ; ++i)
+        if (cm[i].y > 0.f) mr = fmaxf(mr, cm[i].x);
+      const float sa = (wq > 0.f) ? exp2f(mq - mr) : 0.f;  // rescale the earlier rounds
+      wq *= sa;
+      oq = make_float4(oq.x * sa, oq.y * sa, oq.z * sa, oq.w * sa);
+#pragma unroll
+      for (int i = 0; i < kPerQ; ++i) {
+        const float f = (cm[i].y > 0.f) ? exp2f(cm[i].x - mr) : 0.f;
+        wq = fmaf(f, cm[i].y, wq);
+        oq = f4_fma(f, cy[i], oq);
+      }
+      mq = mr;
+    }
+    part[q][d4] = oq;
+    if (d4 == 0) { wm[q] = mq; ww[q] = wq; }
+    __syncthreads();
+    if (tid >= kD / 4) return;
+    M = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (ww[i] > 0.f) M = fmaxf(M, wm[i]);
+    W = 0.f;
+    O = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float f = (ww[i] > 0.f) ? exp2f(wm[i] - M) : 0.f;
+      W = fmaf(f, ww[i], W);
+      O = f4_fma(f, part[i][tid], O);
+    }
+    if (tid == 0) p.merge_count[(long long)seg * R + row] = 0;
+  } else if (tid >= kD / 4) {
+    return;
+  }
+
+  const float inv = W > 0.f ? 1.f / W : 0.f;
+  reinterpret_cast<float4*>(p.out + orow * kD)[tid] = make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
+  if (tid == 0 && p.lse) p.lse[orow] = W > 0.f ? (M + log2f(W)) * kLn2 : -INFINITY;
 }
 
 // ------------------------------------------------------------------ host side
@@ -347,6 +294,30 @@ struct Plan {
   int merge_tasks;
 };
 
+// List the merge tasks (chunks of up to 32 pieces of every segment with more
+// than one piece) into task[]; returns their number, or -1 past kMaxTasks.
+int list_merge_tasks(const int32_t* seq_lens_host, uint32_t n_seq, const Geometry& geo, long long tiles, int ctas,
+                     int2* task) {
+  int n = 0;
+  long long base = 0;
+  for (uint32_t s = 0; s < n_seq; ++s) {
+    const long long ntl = (seq_lens_host[s] + geo.tile_keys - 1) / geo.tile_keys;
+    for (int g = 0; g < geo.segs_per_seq; ++g) {
+      const long long a = base + g * ntl, e = a + ntl - 1;
+      const int c0 = (int)(((a + 1) * ctas - 1) / tiles), c1 = (int)(((e + 1) * ctas - 1) / tiles);
+      const int np = c1 - c0 + 1;
+      if (np < 2) continue;
+      for (int k = 0; k * kChunk < np; ++k) {
+        if (n == kMaxTasks) return -1;
+        if (task) task[n] = make_int2((int)(s * geo.segs_per_seq + g), (c0 << 17) | (k << 11) | np);
+        ++n;
+      }
+    }
+    base += ntl * geo.segs_per_seq;
+  }
+  return n;
+}
+
 // Workspace: piece partials (m, l) and O, the merge's level-1 results of the
 // same shape, and one arrival counter per (segment, row).
 struct WsLayout {
@@ -368,22 +339,6 @@ WsLayout workspace_layout(long long max_ctas, long long n_seg, int R) {
 }
 
 size_t workspace_bytes(long long max_ctas, long long n_seg, int R) { return workspace_layout(max_ctas, n_seg, R).total; }
-
-// Merge tasks: chunks of up to 32 pieces of every segment with more than one piece.
-int merge_tasks(const int32_t* seq_lens_host, uint32_t n_seq, const Geometry& geo, long long tiles, int ctas) {
-  int most = 0;
-  long long base = 0;
-  for (uint32_t s = 0; s < n_seq; ++s) {
-    const long long ntl = (seq_lens_host[s] + geo.tile_keys - 1) / geo.tile_keys;
-    for (int g = 0; g < geo.segs_per_seq; ++g) {
-      const long long a = base + g * ntl, e = a + ntl - 1;
-      const int c0 = (int)(((a + 1) * ctas - 1) / tiles), c1 = (int)(((e + 1) * ctas - 1) / tiles);
-      if (c1 > c0) most += (c1 - c0 + 32) / 32;
-    }
-    base += ntl * geo.segs_per_seq;
-  }
-  return most;
-}
 
 }  // namespace
 
@@ -421,7 +376,12 @@ static pa_status make_plan(const pa_pool_desc& d, const int32_t* seq_lens_host, 
   plan->ctas = (int)std::min<long long>(tiles, (long long)sms * occ);
   plan->n_seg = (long long)n_seq * geo.segs_per_seq;
   plan->slots = (long long)plan->ctas + plan->n_seg;
-  plan->merge_tasks = merge_tasks(seq_lens_host, n_seq, geo, tiles, plan->ctas);
+  // The task word packs c0 < 2^14, chunk < 2^6 and np < 2^11; the task count
+  // is at most about 1.04 x the CTA count (each multi-piece segment holds a
+  // CTA boundary), below kMaxTasks for any grid of fewer than 2000 CTAs.
+  if (plan->ctas >= 2000) return PA_ERR_UNSUPPORTED;
+  plan->merge_tasks = list_merge_tasks(seq_lens_host, n_seq, geo, tiles, plan->ctas, nullptr);
+  if (plan->merge_tasks < 0) return PA_ERR_UNSUPPORTED;
   return PA_OK;
 }
 
@@ -547,6 +507,9 @@ static pa_status run_decode(int passes, PA_DECODE_ARGS) {
     if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
   }
   if ((passes & 2) && plan.merge_tasks > 0) {
+    static thread_local MergeParams mp;  // 8 KB: kept off the stack
+    mp.p = p;
+    list_merge_tasks(seq_lens_host, n_seq, plan.geo, plan.tiles, plan.ctas, mp.task);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)plan.merge_tasks, (unsigned)plan.geo.rows_per_seg);
     cfg.blockDim = dim3(kMergeThreads);
@@ -556,7 +519,7 @@ static pa_status run_decode(int passes, PA_DECODE_ARGS) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, pa_merge_kernel, p) != cudaSuccess) return PA_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, pa_merge_kernel, mp) != cudaSuccess) return PA_ERR_CUDA;
   }
   return PA_OK;
 }
