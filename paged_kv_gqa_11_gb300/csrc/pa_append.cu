@@ -113,7 +113,7 @@ __global__ void pa_wait_selftest_kernel(uint64_t limit_ns, int32_t* err) {
     fence_mbar_init();
   }
   __syncthreads();
-  if (threadIdx.x == 0) mbar_wait(b, 0, err, &abort_flag, false, limit_ns);
+  mbar_wait(b, 0, err, &abort_flag, false, limit_ns);  // the whole (single) warp waits
   __syncthreads();
 }
 

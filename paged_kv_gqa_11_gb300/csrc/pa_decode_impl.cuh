@@ -522,7 +522,7 @@ __device__ void produce_head(const DecodeParams& p, uint32_t ring, uint32_t bar_
 // coalesced float4 loads.  Rows 6 and 7 of the fragment (padding) are zero.
 // Only this warp reads them.
 template <int KT>
-__device__ void stage_q_warp(const DecodeParams& p, int s, int head, uint32_t qf, float* cb4, int lane) {
+__device__ __noinline__ void stage_q_warp(const DecodeParams& p, int s, int head, uint32_t qf, float* cb4, int lane) {
   // zero the padding rows 6, 7 (lanes 24..31 of every k-step) and their biases
   if (lane >= 24) {
 #pragma unroll
@@ -530,12 +530,17 @@ __device__ void stage_q_warp(const DecodeParams& p, int s, int head, uint32_t qf
   }
   if (KT != PA_F16 && lane < 8) sts128_zero(smem_u32(cb4 + (lane * 4 + 3) * 4));
   const float4* q4 = reinterpret_cast<const float4*>(p.q + ((long long)s * p.n_q_heads + head * kGqa) * kD);
-#pragma unroll 4
-  for (int i = 0; i < kGqa * kD / 4 / 32; ++i) {  // 12 float4 per lane
+  // All twelve loads first: they are in flight together (one round trip,
+  // not one per batch), which matters while the bulk copies load HBM.
+  constexpr int kLoads = kGqa * kD / 4 / 32;  // 12 float4 per lane
+  float4 qv[kLoads];
+#pragma unroll
+  for (int i = 0; i < kLoads; ++i) qv[i] = __ldg(q4 + lane + 32 * i);
+#pragma unroll
+  for (int i = 0; i < kLoads; ++i) {
     const int f = lane + 32 * i;
     const int row = f >> 6, d0 = 4 * (f & 63);
-    const float4 v = __ldg(q4 + f);
-    const float vals[4] = {v.x, v.y, v.z, v.w};
+    const float vals[4] = {qv[i].x, qv[i].y, qv[i].z, qv[i].w};
     float lo = 0.f;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
