@@ -45,7 +45,7 @@ FALLBACK_HBM_GBS = 6800.0
 PAGES_PAGED_3090_MS = 4.095
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_split_ragged_q4_0.md")
 DECODE_SOURCES = ["paged_kv_gqa_11_gb300/csrc/pa_decode.cu", "paged_kv_gqa_11_gb300/csrc/pa_decode_impl.cuh",
-                  "paged_kv_gqa_11_gb300/csrc/pa_decode_kern_q4_0.cu", "paged_kv_gqa_11_gb300/csrc/pa_device.cuh",
+                  "paged_kv_gqa_11_gb300/csrc/pa_decode_kern.cu", "paged_kv_gqa_11_gb300/csrc/pa_device.cuh",
                   "paged_kv_gqa_11_gb300/csrc/pa_layout.cuh"]
 
 
@@ -62,6 +62,9 @@ def workload_for(name: str) -> W.Workload:
         return W.config(5, variant="a")
     if name == "many":
         return W.config(5, variant="b")
+    if name.startswith("percall-"):  # percall-<32k|131k|262k>-<1|3|4>: Q8_0 K / Q4_0 V, one sequence
+        _, size, nq = name.split("-")
+        return W.percall({"32k": 32768, "131k": 131072, "262k": 262144}[size], int(nq))
     raise SystemExit(f"unknown workload {name}")
 
 

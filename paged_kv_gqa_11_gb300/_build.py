@@ -17,8 +17,12 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libpa.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["pa_pool.cpp", "pa_append.cu", "pa_decode.cu", "pa_decode_kern_f16.cu", "pa_decode_kern_q4_0.cu",
-           "pa_decode_kern_q8_0.cu"]
+TYPES = {"f16": 1, "q4_0": 2, "q8_0": 8}  # pa_type numbers
+# (source, object name, extra defines): the split-decode kernels are one
+# source compiled once per (K, V) format pair.
+UNITS = [("pa_pool.cpp", "pa_pool", []), ("pa_append.cu", "pa_append", []), ("pa_decode.cu", "pa_decode", [])]
+UNITS += [("pa_decode_kern.cu", f"pa_decode_kern_{k}_{v}", [f"-DPA_KT={TYPES[k]}", f"-DPA_VT={TYPES[v]}"])
+          for k in TYPES for v in TYPES]
 
 
 def _cuda_home() -> str:
@@ -51,13 +55,13 @@ def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(obj_dir, exist_ok=True)
     procs = []
     objs = []
-    for src in SOURCES:
+    for src, name, defs in UNITS:
         path = os.path.join(CSRC, src)
-        obj = os.path.join(obj_dir, src + ".o")
+        obj = os.path.join(obj_dir, name + ".o")
         objs.append(obj)
         if src.endswith(".cu"):
             cmd = [nvcc, *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
-                   "-I", INCLUDE, "-I", CSRC, "-c", path, "-o", obj]
+                   "-I", INCLUDE, "-I", CSRC, *defs, "-c", path, "-o", obj]
             if verbose:
                 cmd.insert(1, "-Xptxas=-v")
         else:

@@ -1,7 +1,7 @@
 // Split-K paged GQA decode: the merge kernel and the host side of pa_decode
 // (validation, planning, launches).  The split kernel itself lives in
-// pa_decode_impl.cuh and is instantiated once per K format in
-// pa_decode_kern_*.cu.
+// pa_decode_impl.cuh and is instantiated in pa_decode_kern.cu, compiled once
+// per (K format, V format) pair.
 //
 // Planning (lucebox PR #555, Summary: context parallelism sized by
 // occupancy): the batch's tiles, counted from the host copy of the sequence
@@ -210,12 +210,13 @@ __global__ void __launch_bounds__(kMergeThreads) pa_merge_kernel(const __grid_co
 // ------------------------------------------------------------------ host side
 
 bool lookup_kernel(int kt, int vt, int nt, KernelInfo* out) {
-  switch (kt) {
-    case PA_F16: return lookup_kernel_f16(vt, nt, out);
-    case PA_Q4_0: return lookup_kernel_q4_0(vt, nt, out);
-    case PA_Q8_0: return lookup_kernel_q8_0(vt, nt, out);
-    default: return false;
-  }
+#define PA_PAIR(k, v) \
+  if (kt == k && vt == v) return lookup_kernel_##k##_##v(nt, out);
+  PA_PAIR(1, 1) PA_PAIR(1, 2) PA_PAIR(1, 8)
+  PA_PAIR(2, 1) PA_PAIR(2, 2) PA_PAIR(2, 8)
+  PA_PAIR(8, 1) PA_PAIR(8, 2) PA_PAIR(8, 8)
+#undef PA_PAIR
+  return false;
 }
 
 int type_slot(int t) { return t == PA_F16 ? 0 : t == PA_Q4_0 ? 1 : t == PA_Q8_0 ? 2 : -1; }

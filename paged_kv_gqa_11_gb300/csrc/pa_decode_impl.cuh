@@ -1306,9 +1306,13 @@ KernelInfo kernel_info() {
   return KernelInfo{pa_split_decode_kernel<KT, VT, NT>, Smem<KT, VT, NT>::kLaunch, CtaTarget<KT, VT, NT>::kN};
 }
 
-// Defined once per K format (one translation unit each).
-bool lookup_kernel_f16(int vt, int nt, KernelInfo* out);
-bool lookup_kernel_q4_0(int vt, int nt, KernelInfo* out);
-bool lookup_kernel_q8_0(int vt, int nt, KernelInfo* out);
+// Defined once per (K, V) format pair, named by the pa_type numbers
+// (pa_decode_kern.cu, one translation unit each).
+#define PA_DECLARE_LOOKUP(k, v) bool lookup_kernel_##k##_##v(int nt, KernelInfo* out);
+PA_DECLARE_LOOKUP(1, 1) PA_DECLARE_LOOKUP(1, 2) PA_DECLARE_LOOKUP(1, 8)
+PA_DECLARE_LOOKUP(2, 1) PA_DECLARE_LOOKUP(2, 2) PA_DECLARE_LOOKUP(2, 8)
+PA_DECLARE_LOOKUP(8, 1) PA_DECLARE_LOOKUP(8, 2) PA_DECLARE_LOOKUP(8, 8)
+#undef PA_DECLARE_LOOKUP
+static_assert(PA_F16 == 1 && PA_Q4_0 == 2 && PA_Q8_0 == 8, "lookup names use the pa_type numbers");
 
 }  // namespace pa_split

@@ -1,0 +1,26 @@
+// Split-decode kernels for one (K format, V format) pair, chosen at compile
+// time with -DPA_KT=<pa_type> -DPA_VT=<pa_type>; the build compiles this file
+// once per pair, so the nine pairs compile in parallel.  Each unit defines
+// lookup_kernel_<K>_<V>, returning the kernel for 1, 2 or 3 n-tiles of query
+// rows (1 token, 2 tokens, 3-4 tokens).
+#include "pa_decode_impl.cuh"
+
+#if !defined(PA_KT) || !defined(PA_VT)
+#error "compile with -DPA_KT=<pa_type> -DPA_VT=<pa_type>"
+#endif
+
+#define PA_LOOKUP_NAME_(k, v) lookup_kernel_##k##_##v
+#define PA_LOOKUP_NAME(k, v) PA_LOOKUP_NAME_(k, v)
+
+namespace pa_split {
+
+bool PA_LOOKUP_NAME(PA_KT, PA_VT)(int nt, KernelInfo* out) {
+  switch (nt) {
+    case 1: *out = kernel_info<PA_KT, PA_VT, 1>(); return true;
+    case 2: *out = kernel_info<PA_KT, PA_VT, 2>(); return true;
+    case 3: *out = kernel_info<PA_KT, PA_VT, 3>(); return true;
+    default: return false;
+  }
+}
+
+}  // namespace pa_split

@@ -49,6 +49,23 @@ def test_small_parity(name, lens, ps, kt, vt, nq, layout):
     assert_lse_close(gl, ol, what=name)
 
 
+PAIRS = [(kt, vt) for kt in (F16, Q4, Q8) for vt in (F16, Q4, Q8)]
+NAMES = {F16: "f16", Q4: "q4_0", Q8: "q8_0"}
+
+
+@pytest.mark.parametrize("kt,vt", PAIRS, ids=[f"k{NAMES[k]}-v{NAMES[v]}" for k, v in PAIRS])
+@pytest.mark.parametrize("nq", [1, 3])
+def test_every_format_pair(kt, vt, nq):
+    """All nine K x V format pairs (Q8_0 K with Q4_0 V is the production
+    pair of lucebox PR #555), one and three query tokens, ragged lengths with
+    partial last tiles and a multi-piece sequence."""
+    w = W.make_workload(f"pair-{kt}-{vt}", 300 + 10 * kt + vt, [2100, 77, 16, 600], 16, kt, vt, nq, "shuffled")
+    go, gl = run_decode(w)
+    oo, ol = oracle.decode_workload(w, n_threads=THREADS)
+    assert_close(go, oo, what=f"k{kt} v{vt} nq{nq}")
+    assert_lse_close(gl, ol, what=f"k{kt} v{vt} nq{nq}")
+
+
 def test_many_short_sequences():
     """More tiles than CTAs: CTAs walk many whole segments and restage Q."""
     rng = np.random.default_rng(9)

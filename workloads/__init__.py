@@ -310,6 +310,19 @@ def config(idx: int, n_qtok: int | None = None, variant: str = "") -> Workload:
     raise ValueError((idx, variant))
 
 
+PERCALL_LENGTHS = (32768, 131072, 262144)
+
+
+def percall(length: int, n_qtok: int) -> Workload:
+    """The per-call shape of the llama.cpp fork's RDNA4 table (PR #2, Q8_0 K
+    scale-read commit): one sequence of 32k / 131k / 262k tokens, Q8_0 K with
+    Q4_0 V, 1 / 3 / 4 query tokens.  The table gives no page size; 256-row
+    pages (the fork's stream pages) in a shuffled pool are a reading."""
+    assert length in PERCALL_LENGTHS and n_qtok in (1, 3, 4)
+    return make_workload(f"percall-{ {32768: 32, 131072: 131, 262144: 262}[length]}k-{n_qtok}", 6, [length], 256, TYPE_Q8_0, TYPE_Q4_0,
+                         n_qtok, "shuffled")
+
+
 def small_workload(seed: int, lengths, ps: int, k_type: int, v_type: int | None = None,
                    n_qtok: int = 1, layout: str = "shuffled") -> Workload:
     """Oracle-sized variants for parity tests (same recipe, smaller lengths)."""
