@@ -1037,7 +1037,14 @@ __device__ void consume_hg(const DecodeParams& p, uint8_t* smem, uint32_t ring, 
 
 // ------------------------------------------------------------------ per-head consumer
 
-// Multi-token path (NT = 2, 3): see the file comment.
+// Multi-token path (NT = 2, 3): see the file comment.  The four warps share
+// one reference maximum per query row (m_ref), so in the common case a tile
+// needs one barrier and no rescaling: each warp computes P for its 16 keys
+// against m_ref and publishes it.  A warp whose logits exceed m_ref by more
+// than 2^8 raises a flag and publishes its per-row base; then (rarely) a
+// second barrier lets every warp form the new maximum, rescale O and its row
+// sums, and scale each warp's P by 2^(base - new).  Row sums are kept per
+// thread over its own keys and reduced once at the end of the piece.
 template <int KT, int VT, int NT>
 __device__ void consume_shared(const DecodeParams& p, uint8_t* smem, uint32_t ring, uint32_t bar_full,
                                uint32_t bar_empty, volatile int* abort, long long a, long long b, int s, int g,
@@ -1050,11 +1057,13 @@ __device__ void consume_shared(const DecodeParams& p, uint8_t* smem, uint32_t ri
   const int gq = lane >> 2, tq = lane & 3;
   const int R = kGqa * p.n_qtok;
   const uint32_t pb_base = ring + SM::kP;
-  float2* stats = reinterpret_cast<float2*>(smem + SM::kStat);
+  float* mbase = reinterpret_cast<float*>(smem + SM::kStat);             // [2][warp][R8] per-row P base
+  int* flags = reinterpret_cast<int*>(smem + SM::kStat + 2 * kCWarps * R8 * 4);  // [2][warp]
   // K row group `warp` and V row group 0 of stage 0, with this lane's offsets.
   const uint32_t kg0 = ring + warp * G::kKGroup, vs0 = ring + G::kKBytes;
   const uint32_t kq0 = kg0 + Fmt<KT>::kScales + lane_chunk_offset<KT>(lane);
   const uint32_t vq_off = Fmt<VT>::kScales + lane_chunk_offset<VT>(lane);
+  const float scale_log2 = p.scale_log2;
   int st = 0;
   uint32_t ph = 0;
   int qbuf = 0, tbuf = 0;
@@ -1079,111 +1088,136 @@ __device__ void consume_shared(const DecodeParams& p, uint8_t* smem, uint32_t ri
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int c = 0; c < 4; ++c) o[i][nt][c] = 0.f;
-    float m_run[NT], l_run[NT];  // for query row nt*8 + gq
+    float m_ref[NT][2], l_part[NT][2];  // rows nt*8 + 2tq + e; l over this thread's keys only
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) { m_run[nt] = -INFINITY; l_run[nt] = 0.f; }
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) { m_ref[nt][e] = -INFINITY; l_part[nt][e] = 0.f; }
 
     const int vis0 = L - p.n_qtok;  // last key visible to query token 0
     for (int jt = jb; jt < je; ++jt) {
-      const uint32_t fb = bar_full + 8 * st;
-      mbar_wait(fb, ph, p.err, abort);
+      mbar_wait(bar_full + 8 * st, ph, p.err, abort);
       const uint32_t so = st * SM::kStageBytes;
       const int k0 = jt * kTile;
       if (k0 + kTile > L) zero_tail_tile<VT>(vs0 + so, L - k0, warp, lane);
 
-      // ---- S phase: the keys of row group `warp`
-      float sacc[NT][4];
+      // ---- S phase: the keys of row group `warp`, all rows
+      float xv[NT][4];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) sacc[nt][c] = 0.f;
-      s_phase<KT, NT>(sacc, kq0 + so, kg0 + so, qf_lane, cb_lane, lane);
+        for (int c = 0; c < 4; ++c) xv[nt][c] = 0.f;
+      s_phase<KT, NT>(xv, kq0 + so, kg0 + so, qf_lane, cb_lane, lane);
       const bool need_mask = (k0 + kTile - 1) > vis0;
       const int key0 = k0 + 16 * warp + gq;
-      float2* st_w = stats + (tbuf * kCWarps + warp) * R8;
+      bool up = false;
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        float xv[4];
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          xv[c] = sacc[nt][c] * p.scale_log2;
+          xv[nt][c] *= scale_log2;
           if (need_mask) {
             const int row = nt * 8 + 2 * tq + (c & 1);
             const int tk = min(row / kGqa, p.n_qtok - 1);
-            const int key = key0 + ((c & 2) ? 8 : 0);
-            if (key > vis0 + tk) xv[c] = -INFINITY;
+            if (key0 + ((c & 2) ? 8 : 0) > vis0 + tk) xv[nt][c] = -INFINITY;
           }
+          up |= xv[nt][c] > m_ref[nt][c & 1] + kLazy;
         }
-        float mx0 = fmaxf(xv[0], xv[2]), mx1 = fmaxf(xv[1], xv[3]);
+      const bool raised = __any_sync(0xffffffffu, up);
+      float* mb_w = mbase + (tbuf * kCWarps + warp) * R8;
+      float base[NT][2];  // this warp's P base per row
 #pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) base[nt][e] = m_ref[nt][e];
+      if (raised) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          float mx0 = fmaxf(xv[nt][0], xv[nt][2]), mx1 = fmaxf(xv[nt][1], xv[nt][3]);
+#pragma unroll
+          for (int off = 4; off < 32; off <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+          }
+          base[nt][0] = fmaxf(base[nt][0], mx0);
+          base[nt][1] = fmaxf(base[nt][1], mx1);
         }
-        const float b0 = (mx0 == -INFINITY) ? 0.f : mx0, b1 = (mx1 == -INFINITY) ? 0.f : mx1;
-        const uint32_t X0 = pack_half2(exp2f(xv[0] - b0), exp2f(xv[1] - b1));
-        const uint32_t X1 = pack_half2(exp2f(xv[2] - b0), exp2f(xv[3] - b1));
-        // Row sums of the fp16-rounded weights (what the PV product uses).
+      }
+      if (lane == 0) flags[tbuf * kCWarps + warp] = raised ? 1 : 0;
+      float rs[NT][2];  // this thread's share of the tile's row sums, relative to base
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const float b0 = (base[nt][0] == -INFINITY) ? 0.f : base[nt][0];
+        const float b1 = (base[nt][1] == -INFINITY) ? 0.f : base[nt][1];
+        const uint32_t X0 = pack_half2(ex2(xv[nt][0] - b0), ex2(xv[nt][1] - b1));
+        const uint32_t X1 = pack_half2(ex2(xv[nt][2] - b0), ex2(xv[nt][3] - b1));
         const float2 f0 = half2_bits_to_float2(X0), f1 = half2_bits_to_float2(X1);
-        float sm0 = f0.x + f1.x, sm1 = f0.y + f1.y;
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-          sm0 += __shfl_xor_sync(0xffffffffu, sm0, off);
-          sm1 += __shfl_xor_sync(0xffffffffu, sm1, off);
-        }
-        if (gq == 0) {
-          st_w[nt * 8 + 2 * tq] = make_float2(mx0, sm0);
-          st_w[nt * 8 + 2 * tq + 1] = make_float2(mx1, sm1);
-        }
+        rs[nt][0] = f0.x + f1.x;
+        rs[nt][1] = f0.y + f1.y;
         const uint32_t B0 = movmatrix_trans(X0), B1 = movmatrix_trans(X1);
         asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(
                          pb_base + (((tbuf * kCWarps + warp) * NT + nt) * 32 + lane) * 8),
                      "r"(B0), "r"(B1)
                      : "memory");
+        if (gq == 0) {
+          mb_w[nt * 8 + 2 * tq] = base[nt][0];
+          mb_w[nt * 8 + 2 * tq + 1] = base[nt][1];
+        }
       }
       named_bar_sync(1, kCWarps * 32);
+      const int4 fl = *reinterpret_cast<const int4*>(flags + tbuf * kCWarps);
+      const bool any_raise = (fl.x | fl.y | fl.z | fl.w) != 0;  // the same in every warp
 
-      // ---- PV phase: dims of m-tiles 4*warp .. +3 over all 64 keys
-      const float2* st_t = stats + tbuf * kCWarps * R8;
-      float fsc[kCWarps][NT];
-      float alpha_c[NT][2];
+      // ---- rare: a new maximum for some rows; fold every warp's base
+      float fsc[kCWarps][NT];  // P scale per producing warp, for query row nt*8 + gq
+      if (any_raise) {
+        const float* mb_t = mbase + tbuf * kCWarps * R8;
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const int row = nt * 8 + gq;
-        float mt[kCWarps], mnew = m_run[nt];
+        for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
-        for (int w2 = 0; w2 < kCWarps; ++w2) {
-          mt[w2] = st_t[w2 * R8 + row].x;
-          mnew = fmaxf(mnew, mt[w2]);
+          for (int e = 0; e < 2; ++e) {
+            const int row = nt * 8 + 2 * tq + e;
+            float mn = m_ref[nt][e];
+#pragma unroll
+            for (int w2 = 0; w2 < kCWarps; ++w2) mn = fmaxf(mn, mb_t[w2 * R8 + row]);
+            const float al = (mn == -INFINITY) ? 1.f : ex2(m_ref[nt][e] - mn);
+            const float fo = (mn == -INFINITY) ? 1.f : ex2(base[nt][e] - mn);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              o[i][nt][e] *= al;
+              o[i][nt][2 + e] *= al;
+            }
+            l_part[nt][e] = l_part[nt][e] * al + rs[nt][e] * fo;
+            m_ref[nt][e] = mn;
+          }
+          const int rg = nt * 8 + gq;
+          float mg = -INFINITY;
+#pragma unroll
+          for (int w2 = 0; w2 < kCWarps; ++w2) mg = fmaxf(mg, mb_t[w2 * R8 + rg]);
+#pragma unroll
+          for (int w2 = 0; w2 < kCWarps; ++w2) fsc[w2][nt] = (mg == -INFINITY) ? 1.f : ex2(mb_t[w2 * R8 + rg] - mg);
         }
-        const float base = (mnew == -INFINITY) ? 0.f : mnew;
-        const float alpha = exp2f(m_run[nt] - base);
-        float lsum = l_run[nt] * alpha;
-#pragma unroll
-        for (int w2 = 0; w2 < kCWarps; ++w2) {
-          fsc[w2][nt] = exp2f(mt[w2] - base);
-          lsum += st_t[w2 * R8 + row].y * fsc[w2][nt];
-        }
-        l_run[nt] = lsum;
-        m_run[nt] = mnew;
-        alpha_c[nt][0] = __shfl_sync(0xffffffffu, alpha, 8 * tq);      // row 2*tq lives at g = 2*tq
-        alpha_c[nt][1] = __shfl_sync(0xffffffffu, alpha, 8 * tq + 4);  // row 2*tq+1
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
+      } else {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int c = 0; c < 4; ++c) o[i][nt][c] *= alpha_c[nt][c & 1];
+          for (int e = 0; e < 2; ++e) l_part[nt][e] += rs[nt][e];
+      }
+
+      // ---- PV phase: dims of m-tiles 4*warp .. +3 over all 64 keys
 #pragma unroll
       for (int kw = 0; kw < kCWarps; ++kw) {
         uint32_t bp[NT][2];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           const uint2 v = lds64(pb_base + (((tbuf * kCWarps + kw) * NT + nt) * 32 + lane) * 8);
-          const uint32_t f2 = pack_half2(fsc[kw][nt], fsc[kw][nt]);
-          bp[nt][0] = hmul2(v.x, f2);
-          bp[nt][1] = hmul2(v.y, f2);
+          bp[nt][0] = v.x;
+          bp[nt][1] = v.y;
+          if (any_raise) {
+            const uint32_t f2 = pack_half2(fsc[kw][nt], fsc[kw][nt]);
+            bp[nt][0] = hmul2(v.x, f2);
+            bp[nt][1] = hmul2(v.y, f2);
+          }
         }
         const uint32_t vg = vs0 + so + kw * G::kVGroup;
         pv_kstep<VT, NT>(o, vg + vq_off, vg, warp, lane, bp);
@@ -1194,19 +1228,28 @@ __device__ void consume_shared(const DecodeParams& p, uint8_t* smem, uint32_t ri
       tbuf ^= 1;
     }
 
-    // ---- end of piece: final output or a split partial
+    // ---- end of piece: row sums over the warp's lanes, then over the warps
+    float* lsum = mbase + tbuf * kCWarps * R8;  // the buffer the next tile would write first
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float v = l_part[nt][e];
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+        if (gq == 0) lsum[warp * R8 + nt * 8 + 2 * tq + e] = v;
+      }
+    named_bar_sync(1, kCWarps * 32);
     const int slot = (int)blockIdx.x + seg;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const float lc0 = __shfl_sync(0xffffffffu, l_run[nt], 8 * tq);
-      const float lc1 = __shfl_sync(0xffffffffu, l_run[nt], 8 * tq + 4);
-      const float mc0 = __shfl_sync(0xffffffffu, m_run[nt], 8 * tq);
-      const float mc1 = __shfl_sync(0xffffffffu, m_run[nt], 8 * tq + 4);
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         const int row = nt * 8 + 2 * tq + c;
         if (row >= R) continue;
-        const float lr = c ? lc1 : lc0;
+        float lr = 0.f;
+#pragma unroll
+        for (int w2 = 0; w2 < kCWarps; ++w2) lr += lsum[w2 * R8 + row];
         float* dst = row_dst(p, whole, slot, s, g, row, R);
         const float inv = whole ? (lr > 0.f ? 1.f / lr : 0.f) : 1.f;
 #pragma unroll
@@ -1214,9 +1257,10 @@ __device__ void consume_shared(const DecodeParams& p, uint8_t* smem, uint32_t ri
           dst[vdim<VT>(gq, 4 * warp + i, 0)] = o[i][nt][c] * inv;
           dst[vdim<VT>(gq, 4 * warp + i, 1)] = o[i][nt][2 + c] * inv;
         }
-        if (warp == 0 && gq == 0) write_row_stats(p, whole, slot, s, g, row, R, c ? mc1 : mc0, lr);
+        if (warp == 0 && gq == 0) write_row_stats(p, whole, slot, s, g, row, R, m_ref[nt][c], lr);
       }
     }
+    named_bar_sync(1, kCWarps * 32);  // lsum is read before the next piece's tiles reuse it
 
     x += je - jb;
     qbuf ^= 1;
