@@ -577,55 +577,73 @@ __device__ __forceinline__ const float* q_row(const DecodeParams& p, int s, int 
   return p.q + (((long long)s * p.n_qtok + tq) * p.n_q_heads + g * kGqa + hl) * kD;
 }
 
-__device__ __forceinline__ float round_half(float v) { return __half2float(__float2half_rn(v)); }
-
-// Block bias c of query row `row` for block blk (0 past the real rows).
-template <int KT>
-__device__ __forceinline__ float block_bias(const DecodeParams& p, int s, int g, int row, int R, int blk) {
-  if (row >= R) return 0.f;
-  const float* qr = q_row(p, s, g, row) + 32 * blk;
-  float lo = 0.f, hi = 0.f;
-#pragma unroll 8
-  for (int i = 0; i < 16; ++i) lo += round_half(__ldg(qr + i));
-  if constexpr (KT == PA_Q4_0) {
-#pragma unroll 8
-    for (int i = 16; i < 32; ++i) hi += round_half(0.0625f * __ldg(qr + i));
-    return 1032.f * lo + 1152.f * hi;
-  } else {
-#pragma unroll 8
-    for (int i = 16; i < 32; ++i) lo += round_half(__ldg(qr + i));
-    return 1152.f * lo;
-  }
-}
 
 // Per-head path: stage Q of (sequence s, KV head g) as S-MMA B fragments in
 // the K format's dim order (high-nibble Q4_0 k-steps hold Q/16) and, for
 // quantised K, the block biases ([block][nt][t] float4).  All consumer
-// threads take part.
+// threads take part: the R query rows (1 KB each) are read as float4, all of
+// a thread's loads in flight at once; rows R .. 8*NT-1 of the fragments and
+// biases are zero.
 template <int KT, int NT>
-__device__ void stage_q(const DecodeParams& p, int s, int g, uint32_t qf, float* cb4, int tid) {
+__device__ __noinline__ void stage_q(const DecodeParams& p, int s, int g, uint32_t qf, float* cb4, int tid) {
   const int R = kGqa * p.n_qtok;
   constexpr int kN = kCWarps * 32;
-  for (int e = tid; e < 16 * NT * 32; e += kN) {
-    const int ln = e & 31, nt = (e >> 5) % NT, ks = e / (32 * NT);
-    const int row = nt * 8 + (ln >> 2), t4 = ln & 3;
-    uint32_t b0 = 0, b1 = 0;
-    if (row < R) {
-      const float* qr = q_row(p, s, g, row);
-      const float f = (KT == PA_Q4_0 && (ks & 1)) ? 0.0625f : 1.f;
-      b0 = pack_half2(f * __ldg(qr + kdim<KT>(ks, 2 * t4)), f * __ldg(qr + kdim<KT>(ks, 2 * t4 + 1)));
-      b1 = pack_half2(f * __ldg(qr + kdim<KT>(ks, 2 * t4 + 8)), f * __ldg(qr + kdim<KT>(ks, 2 * t4 + 9)));
-    }
-    asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(qf + (((ks >> 1) * NT + nt) * 32 + ln) * 16 + (ks & 1) * 8),
-                 "r"(b0), "r"(b1)
-                 : "memory");
+  constexpr int kLoads = (NT * 8 * kD / 4 + kN - 1) / kN;  // float4 per thread covering 8*NT rows
+  const int lane = tid & 31;
+  // zero the padding rows: fragment lanes (row % 8) * 4 + t of n-tile row / 8
+  for (int e = tid; e < 8 * NT * 32; e += kN) {  // (k-step pair, nt, lane)
+    const int ln = e & 31, nt = (e >> 5) % NT, kp = e / (32 * NT);
+    if (nt * 8 + (ln >> 2) >= R) sts128_zero(qf + ((kp * NT + nt) * 32 + ln) * 16);
   }
   if (KT != PA_F16) {
-    for (int e = tid; e < 8 * NT * 4; e += kN) {
-      const int blk = e / (NT * 4), nt = (e / 4) % NT, t = e % 4;
-      const float c0 = block_bias<KT>(p, s, g, nt * 8 + 2 * t, R, blk);
-      const float c1 = block_bias<KT>(p, s, g, nt * 8 + 2 * t + 1, R, blk);
-      reinterpret_cast<float4*>(cb4)[e] = make_float4(-c0, -c1, -c0, -c1);
+    for (int e = tid; e < 8 * NT * 8; e += kN) {  // (block, row) pairs of padding rows
+      const int blk = e / (NT * 8), row = e % (NT * 8);
+      if (row >= R) {
+        float* c = cb4 + ((blk * NT + (row >> 3)) * 4 + ((row & 7) >> 1)) * 4 + (row & 1);
+        c[0] = 0.f;
+        c[2] = 0.f;
+      }
+    }
+  }
+  float4 qv[kLoads];
+#pragma unroll
+  for (int i = 0; i < kLoads; ++i) {
+    const int f = tid + kN * i, row = f >> 6;
+    qv[i] = row < R ? __ldg(reinterpret_cast<const float4*>(q_row(p, s, g, row)) + (f & 63))
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+#pragma unroll
+  for (int i = 0; i < kLoads; ++i) {
+    const int f = tid + kN * i, row = f >> 6, d0 = 4 * (f & 63);
+    const float vals[4] = {qv[i].x, qv[i].y, qv[i].z, qv[i].w};
+    float lo = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      int ks, jj;
+      const int t = kdim_inverse<KT>(d0 + k, ks, jj);
+      const float sc = (KT == PA_Q4_0 && (ks & 1)) ? 0.0625f : 1.f;
+      const __half hv = __float2half_rn(sc * vals[k]);
+      lo += __half2float(hv);
+      if (row < R) {
+        const int ln = 4 * (row & 7) + t;
+        const uint32_t addr =
+            qf + (((ks >> 1) * NT + (row >> 3)) * 32 + ln) * 16 + (ks & 1) * 8 + ((jj >> 3) << 2) + ((jj & 1) << 1);
+        asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(__half_as_ushort(hv)) : "memory");
+      }
+    }
+    if (KT != PA_F16) {
+      // Lanes 8m .. 8m+7 hold the eight float4 of one 32-dim block of one row
+      // (k < 4: its low 16 dims, k >= 4: its high 16 dims).
+      lo += __shfl_xor_sync(0xffffffffu, lo, 1);
+      lo += __shfl_xor_sync(0xffffffffu, lo, 2);
+      const float hi = __shfl_down_sync(0xffffffffu, lo, 4);
+      if ((lane & 7) == 0 && row < R) {
+        const int blk = (f & 63) >> 3;
+        const float c = (KT == PA_Q4_0) ? 1032.f * lo + 1152.f * hi : 1152.f * (lo + hi);
+        float* e = cb4 + ((blk * NT + (row >> 3)) * 4 + ((row & 7) >> 1)) * 4 + (row & 1);
+        e[0] = -c;
+        e[2] = -c;
+      }
     }
   }
 }
