@@ -290,6 +290,53 @@ def run_reference(args, w: W.Workload):
     print(json.dumps(line), flush=True)
 
 
+def run_append(args, w: W.Workload):
+    """Quantise-on-append throughput: every row of the workload, given as
+    binary16, quantised into the workload's K/V formats and scattered through
+    its table, per call; bytes = fp16 rows read + pool bytes written."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from paged_kv_gqa_11_gb300.cache import PagedKVCache
+    dev = torch.device("cuda", 0)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    c = PagedKVCache(w.n_blocks, w.page_size, w.k_type, w.v_type, device=dev)
+    n = int(w.row_seq.shape[0])
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    hk = torch.randn((n, W.HKV, W.D), generator=g, device=dev).half()
+    hv = torch.randn((n, W.HKV, W.D), generator=g, device=dev).half()
+    rs, rp, tab = t(w.row_seq), t(w.row_pos), t(w.table)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        c.append_f16(hk, hv, rs, rp, tab, stream=stream.cuda_stream)
+    torch.cuda.synchronize()
+    if c.check() != 0:
+        raise SystemExit("append reported a device error")
+    K = min(args.steps, 200)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    for i in range(K):
+        flush.fill_(1.0)
+        ev[i][0].record(stream)
+        c.append_f16(hk, hv, rs, rp, tab, stream=stream.cuda_stream)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in range(K))
+    nbytes = n * W.HKV * (2 * W.D * 2 + W.row_bytes(w.k_type) + W.row_bytes(w.v_type))
+    peaks = measured_peaks()
+    peak = float(peaks["hbm_gbs"]) if peaks and "hbm_gbs" in peaks else FALLBACK_HBM_GBS
+    gbps = nbytes / (ms * 1e-3) / 1e9
+    print(json.dumps({
+        "metric": "quantise-on-append GB/s (binary16 rows read + pool bytes written)", "value": round(gbps, 2),
+        "unit": "GB/s", "n_gpus": 1, "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": describe(w) + f"; {n} rows appended per call", "bytes_per_step": nbytes},
+        "roofline": {"bound": "hbm", "achieved": round(gbps, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(gbps / peak, 4), "traffic": None}}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -300,6 +347,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--mode", choices=["decode", "append"], default="decode",
+                    help="append: time quantise-on-append (pa_append_rows_f16) instead of decode")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
@@ -307,6 +356,9 @@ def main():
     w = workload_for(args.workload)
     if args.impl == "reference":
         run_reference(args, w)
+        return
+    if args.mode == "append":
+        run_append(args, w)
         return
 
     import torch

@@ -131,10 +131,10 @@ pa_status pa_block_index(const pa_pool* pool, pa_block handle, int32_t* idx);
 uint32_t pa_pool_free_count(const pa_pool* pool);
 
 /* ------------------------------------------------------------------ append
- * Upload newly appended rows once, then scatter them into their page slots
- * ("upload only newly appended KV rows through one packed transfer and
- * scatter kernel" -- colibri PR #372, Summary; "writes map cells to pool rows
- * through k/v idxs" -- llama.cpp fork PR #2, KV-pool commit).
+ * New rows are uploaded once, packed, and a kernel scatters them into their
+ * page slots (colibri PR #372, Summary: one packed transfer of the newly
+ * appended rows plus a scatter kernel; llama.cpp fork PR #2, KV-pool commit:
+ * cache writes reach pool rows through index tensors).
  *
  * k_rows, v_rows: device, packed [n_rows][n_kv_heads][row_bytes], already in
  *                 storage format; 16-byte aligned.
@@ -152,6 +152,26 @@ pa_status pa_append_rows(const pa_pool* pool, void* k_pool, void* v_pool, const 
                          const void* v_rows, const int32_t* row_seq, const int32_t* row_pos,
                          uint32_t n_rows, const int32_t* block_table, uint32_t table_stride,
                          uint32_t n_seq, int32_t* err, pa_stream_t stream);
+
+/* Quantise on append: the same scatter, from rows given as IEEE binary16
+ * values, converted to the pool's K and V formats on the way in (a cache
+ * write into quantised pages, as the llama.cpp fork's pool writes do; the
+ * pages print no rule, so the rule is ggml's reference quantiser, a
+ * reading).  Per 32-value block, in float32 with every operation rounded on
+ * its own (no fused multiply-add):
+ *   Q8_0: d = max|x| / 127, id = d ? 1/d : 0, q = round-half-away(x * id);
+ *   Q4_0: m = the x of largest |x| (the first on ties), d = m / -8,
+ *         id = d ? 1/d : 0, q = min(15, trunc(x * id + 8.5));
+ *   both store fp16(d), rounded to nearest even; F16 pools take the values
+ *   as they are.
+ * k_rows, v_rows: device binary16 [n_rows][n_kv_heads][head_dim], 16-byte
+ * aligned, finite values.  Everything else as pa_append_rows; the bytes
+ * written equal those of quantising each block with the rule above and
+ * appending the result with pa_append_rows. */
+pa_status pa_append_rows_f16(const pa_pool* pool, void* k_pool, void* v_pool, const uint16_t* k_rows,
+                             const uint16_t* v_rows, const int32_t* row_seq, const int32_t* row_pos,
+                             uint32_t n_rows, const int32_t* block_table, uint32_t table_stride,
+                             uint32_t n_seq, int32_t* err, pa_stream_t stream);
 
 /* ------------------------------------------------------------------ decode
  * Single-step GQA decode attention over a paged cache: split-K flash decoding

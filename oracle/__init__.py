@@ -105,6 +105,10 @@ def _load(path):
     L.orc_scatter.restype = C.c_int
     L.orc_scatter.argtypes = [C.c_void_p, C.c_long, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int,
                               C.c_void_p, C.c_void_p, C.c_void_p, C.c_long, C.c_void_p, C.c_long, C.c_int]
+    L.orc_float_to_half.restype = C.c_uint16
+    L.orc_float_to_half.argtypes = [C.c_float]
+    L.orc_quantize_block.restype = C.c_int
+    L.orc_quantize_block.argtypes = [C.c_int, C.c_void_p, C.c_void_p]
     L.orc_group_offset.restype = C.c_long
     L.orc_group_offset.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int, C.c_long]
     return L
@@ -157,6 +161,28 @@ def dequant_rows(rows: np.ndarray, t: int, d: int = 256) -> np.ndarray:
         if rc:
             raise ValueError(f"orc_dequant_row rc={rc}")
     return out.reshape(*rows.shape[:-1], d)
+
+
+def float_to_half(x) -> np.ndarray:
+    """float32 values -> binary16 bit patterns (uint16), round to nearest even."""
+    L = lib()
+    xs = np.asarray(x, dtype=np.float32).ravel()
+    return np.array([L.orc_float_to_half(float(v)) for v in xs], dtype=np.uint16).reshape(np.shape(x))
+
+
+def quantize_rows(half_bits: np.ndarray, t: int) -> np.ndarray:
+    """binary16 rows (uint16 [..., d]) -> rows in format t (uint8 [..., row_bytes]),
+    one 32-value block at a time with the oracle's quantiser."""
+    L = lib()
+    h = np.ascontiguousarray(half_bits, dtype=np.uint16)
+    d = h.shape[-1]
+    blocks = h.reshape(-1, 32)
+    bb = {F16: 64, Q4_0: 18, Q8_0: 34}[t]
+    out = np.empty((blocks.shape[0], bb), np.uint8)
+    for i in range(blocks.shape[0]):
+        if L.orc_quantize_block(t, _ptr(blocks[i]), _ptr(out[i])) != bb:
+            raise ValueError("orc_quantize_block")
+    return out.reshape(*h.shape[:-1], d // 32 * bb)
 
 
 def group_offset(t: int, role: int, r: int, i: int, d: int = 256) -> int:

@@ -117,6 +117,92 @@ int orc_dequant_row(int type, const uint8_t* row, int d, double* out) {
   return ORC_OK;
 }
 
+/* float -> IEEE binary16 bits, rounding to nearest, ties to even; overflow
+ * gives infinity, NaN stays NaN.  Written from the binary16 format
+ * definition (1 sign, 5 exponent bits biased by 15, 10 fraction bits). */
+uint16_t orc_float_to_half(float f) {
+  uint32_t x;
+  memcpy(&x, &f, 4);
+  const uint16_t sign = (uint16_t)((x >> 16) & 0x8000u);
+  const int e = (int)((x >> 23) & 0xff);
+  const uint32_t frac = x & 0x7fffffu;
+  if (e == 255) return (uint16_t)(sign | 0x7c00u | (frac ? 0x200u : 0u));
+  /* value = 1.frac * 2^(e-127); binary16 keeps exponents -14 .. 15 normal */
+  const int he = e - 127 + 15;
+  if (he >= 31) return (uint16_t)(sign | 0x7c00u);
+  uint32_t mant, shift;
+  if (he >= 1) {           /* normal: keep 10 of the 23 fraction bits */
+    mant = (1u << 23) | frac;
+    shift = 13;
+  } else {                 /* subnormal or zero: units of 2^-24 */
+    if (e == 0 || he < -10) return sign;  /* below half of the smallest subnormal */
+    mant = (1u << 23) | frac;
+    shift = (uint32_t)(14 - he);          /* 13 + (1 - he) */
+  }
+  uint32_t q = mant >> shift;
+  const uint32_t rem = mant & ((1u << shift) - 1u), half = 1u << (shift - 1);
+  if (rem > half || (rem == half && (q & 1u))) ++q;
+  if (he >= 1) {
+    /* q holds 1.f in 11 bits; a carry to 2^11 moves to the next exponent */
+    uint32_t exp = (uint32_t)he;
+    if (q >> 11) { q >>= 1; ++exp; }
+    if (exp >= 31) return (uint16_t)(sign | 0x7c00u);
+    return (uint16_t)(sign | (exp << 10) | (q & 0x3ffu));
+  }
+  return (uint16_t)(sign | q); /* q == 0x400 becomes the smallest normal, correctly */
+}
+
+/* Quantise one 32-value block given as binary16 bits, as ggml's reference
+ * quantisers do (a reading: the pages write new cells into quantised cache
+ * pages without printing the rule), in float32 with no fused operations:
+ *   Q8_0: amax = max |x|; d = amax / 127; id = d ? 1/d : 0;
+ *         q = round-half-away(x * id); bytes: fp16(d), then 32 int8 q.
+ *   Q4_0: m = the x of largest |x| (the first on ties); d = m / -8;
+ *         id = d ? 1/d : 0; q = min(15, trunc(x * id + 8.5));
+ *         bytes: fp16(d), then byte j = q_j | q_(j+16) << 4.
+ * F16 blocks are copied.  Returns the block's byte count, or -1. */
+int orc_quantize_block(int type, const uint16_t* h, uint8_t* out) {
+  float x[32];
+  for (int i = 0; i < 32; ++i) x[i] = (float)orc_half_to_double(h[i]);
+  if (type == ORC_F16) {
+    memcpy(out, h, 64);
+    return 64;
+  }
+  if (type == ORC_Q8_0) {
+    float amax = 0.0f;
+    for (int i = 0; i < 32; ++i) amax = fabsf(x[i]) > amax ? fabsf(x[i]) : amax;
+    const float d = amax / 127.0f;
+    const float id = d != 0.0f ? 1.0f / d : 0.0f;
+    const uint16_t dh = orc_float_to_half(d);
+    out[0] = (uint8_t)(dh & 0xff);
+    out[1] = (uint8_t)(dh >> 8);
+    for (int i = 0; i < 32; ++i) {
+      const float v = x[i] * id;
+      out[2 + i] = (uint8_t)(int8_t)roundf(v);
+    }
+    return 34;
+  }
+  if (type == ORC_Q4_0) {
+    float amax = 0.0f, m = 0.0f;
+    for (int i = 0; i < 32; ++i)
+      if (fabsf(x[i]) > amax) { amax = fabsf(x[i]); m = x[i]; }
+    const float d = m / -8.0f;
+    const float id = d != 0.0f ? 1.0f / d : 0.0f;
+    const uint16_t dh = orc_float_to_half(d);
+    out[0] = (uint8_t)(dh & 0xff);
+    out[1] = (uint8_t)(dh >> 8);
+    int q[32];
+    for (int i = 0; i < 32; ++i) {
+      const float v = x[i] * id + 8.5f;
+      const int t = (int)truncf(v);
+      q[i] = t < 15 ? t : 15;
+    }
+    for (int j = 0; j < 16; ++j) out[2 + j] = (uint8_t)(q[j] | (q[j + 16] << 4));
+    return 18;
+  }
+  return -1;
+}
+
 /* Pool layout.  A pool is [block][kv_head][page_size rows] with page_size a
  * multiple of ORC_GROUP (16); each page is cut into groups of 16 consecutive
  * slots, and a group stores its 16 rows in 16 * row_bytes bytes, arranged for

@@ -18,7 +18,7 @@ import threading
 from . import _build
 
 __all__ = [
-    "PA_F16", "PA_Q4_0", "PA_Q8_0", "PaError", "Pool", "load", "row_bytes", "pa_append_rows", "pa_decode",
+    "PA_F16", "PA_Q4_0", "PA_Q8_0", "PaError", "Pool", "load", "row_bytes", "pa_append_rows", "pa_append_rows_f16", "pa_decode",
     "pa_decode_workspace_size", "pa_decode_plan", "pa_get_error", "pa_selftest_wait_timeout", "status_name",
     "library_path", "pa_decode_noalloc",
 ]
@@ -30,7 +30,7 @@ PA_OK, PA_ERR_INVALID, PA_ERR_UNSUPPORTED, PA_ERR_OOM, PA_ERR_STALE, PA_ERR_BOUN
 
 # Every entry point declared in include/pa.h.
 EXPORTS = ["pa_pool_create", "pa_pool_destroy", "pa_pool_get_desc", "pa_row_bytes", "pa_pool_bytes",
-           "pa_alloc_blocks", "pa_release", "pa_block_index", "pa_pool_free_count", "pa_append_rows",
+           "pa_alloc_blocks", "pa_release", "pa_block_index", "pa_pool_free_count", "pa_append_rows", "pa_append_rows_f16",
            "pa_decode", "pa_decode_split", "pa_decode_merge", "pa_decode_workspace_size", "pa_decode_plan", "pa_get_error", "pa_status_string",
            "pa_selftest_wait_timeout", "pa_decode_noalloc"]
 
@@ -80,6 +80,7 @@ def load():
             "pa_block_index": (C.c_int, [vp, C.c_uint64, C.POINTER(i32)]),
             "pa_pool_free_count": (u32, [vp]),
             "pa_append_rows": (C.c_int, [vp, vp, vp, vp, vp, vp, vp, u32, vp, u32, u32, vp, vp]),
+            "pa_append_rows_f16": (C.c_int, [vp, vp, vp, vp, vp, vp, vp, u32, vp, u32, u32, vp, vp]),
             "pa_decode": (C.c_int, [vp, vp, vp, vp, vp, u32, vp, vp, u32, u32, u32, C.c_float, vp, vp, vp, sz,
                                     vp, vp]),
             "pa_decode_workspace_size": (sz, [vp, u32, u32, C.c_int]),
@@ -190,6 +191,15 @@ def pa_append_rows(pool: Pool, k_pool, v_pool, k_rows, v_rows, row_seq, row_pos,
                                _ptr(row_pos), n_rows, _ptr(block_table), table_stride, n_seq, _ptr(err),
                                _stream(stream))
     _check(rc, "pa_append_rows")
+
+
+def pa_append_rows_f16(pool: Pool, k_pool, v_pool, k_rows, v_rows, row_seq, row_pos, n_rows: int, block_table,
+                       table_stride: int, n_seq: int, err, stream=None) -> None:
+    """Rows as binary16 [n_rows][n_kv_heads][head_dim], quantised into the pool's formats."""
+    rc = load().pa_append_rows_f16(pool.handle, _ptr(k_pool), _ptr(v_pool), _ptr(k_rows), _ptr(v_rows),
+                                   _ptr(row_seq), _ptr(row_pos), n_rows, _ptr(block_table), table_stride, n_seq,
+                                   _ptr(err), _stream(stream))
+    _check(rc, "pa_append_rows_f16")
 
 
 def pa_decode_workspace_size(pool: Pool, n_seq: int, n_qtok: int, device: int = 0) -> int:

@@ -10,7 +10,8 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from . import PA_OK, PaError, Pool, load, pa_append_rows, pa_decode, pa_decode_workspace_size, pa_get_error
+from . import (PA_OK, PaError, Pool, load, pa_append_rows, pa_append_rows_f16, pa_decode, pa_decode_workspace_size,
+               pa_get_error)
 
 
 class PagedKVCache:
@@ -38,6 +39,14 @@ class PagedKVCache:
         n = int(row_seq.shape[0])
         pa_append_rows(self.pool, self.k_pool, self.v_pool, k_rows, v_rows, row_seq, row_pos, n, block_table,
                        int(block_table.shape[1]), int(block_table.shape[0]), self.err, stream)
+
+    def append_f16(self, k_rows: torch.Tensor, v_rows: torch.Tensor, row_seq: torch.Tensor, row_pos: torch.Tensor,
+                   block_table: torch.Tensor, stream=None) -> None:
+        """Quantise binary16 rows [n][n_kv_heads][head_dim] (device, float16 or their uint16
+        bit patterns) into the pools' formats while scattering them."""
+        n = int(row_seq.shape[0])
+        pa_append_rows_f16(self.pool, self.k_pool, self.v_pool, k_rows, v_rows, row_seq, row_pos, n, block_table,
+                           int(block_table.shape[1]), int(block_table.shape[0]), self.err, stream)
 
     # ------------------------------------------------------------ decode
     def workspace(self, n_seq: int, n_qtok: int) -> torch.Tensor:

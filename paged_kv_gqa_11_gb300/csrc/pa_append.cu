@@ -10,6 +10,7 @@
 // 32-value block of a quantised row (one 16- or two 32-byte chunk stores and a
 // 2-byte scale) or one 16-byte chunk of an F16 row; a warp covers consecutive
 // units of consecutive rows.
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -22,6 +23,8 @@ using namespace pa_dev;
 using namespace pa_layout;
 
 namespace {
+
+constexpr int kD_append = 256;  // values per row (the pool requires head_dim 256)
 
 struct AppendParams {
   uint8_t* k_pool;
@@ -70,7 +73,83 @@ __device__ __forceinline__ void place_unit(int type, bool role_v, const uint8_t*
   *reinterpret_cast<uint16_t*>(grp + (role_v ? v_scale_offset(r, u) : k_scale_offset(r, u))) = (uint16_t)d;
 }
 
-// One thread per unit of the packed input; K units first, then V.
+// Quantise-on-append: block u (32 values) of a binary16 row, converted to
+// the pool's format and placed.  The rule is ggml's reference quantiser in
+// float32, every operation rounded on its own (no fused multiply-add):
+//   Q8_0: d = max|x| / 127, id = d ? 1/d : 0, q = round-half-away(x * id);
+//   Q4_0: m = the x of largest |x| (first on ties), d = m / -8,
+//         id = d ? 1/d : 0, q = min(15, trunc(x * id + 8.5)), byte j =
+//         q_j | q_(j+16) << 4;
+//   the scale is stored as fp16(d), rounded to nearest even.
+__device__ __forceinline__ void place_block_f16(int type, bool role_v, const uint8_t* src_row, uint8_t* grp, int r,
+                                                int u) {
+  const uint4* s4 = reinterpret_cast<const uint4*>(src_row + 64 * u);
+  uint4 c[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) c[k] = __ldg(s4 + k);
+  if (type == PA_F16) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      *reinterpret_cast<uint4*>(grp + chunk_offset(0, Fmt<PA_F16>::kRowQ, r, 4 * u + k)) = c[k];
+    return;
+  }
+  float x[32];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t w[4] = {c[k].x, c[k].y, c[k].z, c[k].w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      x[8 * k + 2 * i] = __half2float(__ushort_as_half((unsigned short)(w[i] & 0xffffu)));
+      x[8 * k + 2 * i + 1] = __half2float(__ushort_as_half((unsigned short)(w[i] >> 16)));
+    }
+  }
+  float d;
+  if (type == PA_Q8_0) {
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(x[i]));
+    d = __fdiv_rn(amax, 127.f);
+    const float id = d != 0.f ? __fdiv_rn(1.f, d) : 0.f;
+    uint32_t wq[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      uint32_t v = 0;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) v |= ((uint32_t)(uint8_t)(int8_t)(int)roundf(__fmul_rn(x[4 * j + b], id))) << (8 * b);
+      wq[j] = v;
+    }
+    *reinterpret_cast<uint4*>(grp + chunk_offset(256, Fmt<PA_Q8_0>::kRowQ, r, 2 * u)) =
+        make_uint4(wq[0], wq[1], wq[2], wq[3]);
+    *reinterpret_cast<uint4*>(grp + chunk_offset(256, Fmt<PA_Q8_0>::kRowQ, r, 2 * u + 1)) =
+        make_uint4(wq[4], wq[5], wq[6], wq[7]);
+  } else {  // Q4_0
+    float amax = 0.f, m = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (fabsf(x[i]) > amax) { amax = fabsf(x[i]); m = x[i]; }
+    d = __fdiv_rn(m, -8.f);
+    const float id = d != 0.f ? __fdiv_rn(1.f, d) : 0.f;
+    int q[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) q[i] = min((int)truncf(__fadd_rn(__fmul_rn(x[i], id), 8.5f)), 15);
+    uint32_t wq[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t v = 0;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) v |= (uint32_t)(q[4 * j + b] | (q[4 * j + b + 16] << 4)) << (8 * b);
+      wq[j] = v;
+    }
+    *reinterpret_cast<uint4*>(grp + chunk_offset(256, Fmt<PA_Q4_0>::kRowQ, r, u)) = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+  }
+  *reinterpret_cast<uint16_t*>(grp + (role_v ? v_scale_offset(r, u) : k_scale_offset(r, u))) =
+      __half_as_ushort(__float2half_rn(d));
+}
+
+// One thread per unit of the packed input; K units first, then V.  kF16In:
+// the input rows are binary16 [n_rows][n_kv_heads][head_dim] and every unit
+// is a 32-value block, quantised to the pool's format.
+template <bool kF16In>
 __global__ void __launch_bounds__(256) pa_append_kernel(const __grid_constant__ AppendParams p) {
   const long long k_total = p.n_rows * p.n_kv_heads * p.k_units;
   const long long v_total = p.n_rows * p.n_kv_heads * p.v_units;
@@ -98,8 +177,13 @@ __global__ void __launch_bounds__(256) pa_append_kernel(const __grid_constant__ 
     const int slot = pos % p.page_size;
     const long long grp_row = ((long long)blk * p.n_kv_heads + h) * p.page_size + (slot & ~(kGroup - 1));
     uint8_t* grp = (is_k ? p.k_pool : p.v_pool) + grp_row * rb;
-    const uint8_t* src = (is_k ? p.k_rows : p.v_rows) + rh * rb;
-    place_unit(is_k ? p.k_type : p.v_type, !is_k, src, grp, slot & (kGroup - 1), u);
+    if constexpr (kF16In) {
+      const uint8_t* src = (is_k ? p.k_rows : p.v_rows) + rh * (2 * kD_append);
+      place_block_f16(is_k ? p.k_type : p.v_type, !is_k, src, grp, slot & (kGroup - 1), u);
+    } else {
+      const uint8_t* src = (is_k ? p.k_rows : p.v_rows) + rh * rb;
+      place_unit(is_k ? p.k_type : p.v_type, !is_k, src, grp, slot & (kGroup - 1), u);
+    }
   }
 }
 
@@ -119,10 +203,11 @@ __global__ void pa_wait_selftest_kernel(uint64_t limit_ns, int32_t* err) {
 
 }  // namespace
 
-extern "C" pa_status pa_append_rows(const pa_pool* pool, void* k_pool, void* v_pool, const void* k_rows,
-                                    const void* v_rows, const int32_t* row_seq, const int32_t* row_pos,
-                                    uint32_t n_rows, const int32_t* block_table, uint32_t table_stride,
-                                    uint32_t n_seq, int32_t* err, pa_stream_t stream) {
+// Host validation and launch shared by both append entry points.
+static pa_status launch_append(bool f16_in, const pa_pool* pool, void* k_pool, void* v_pool, const void* k_rows,
+                               const void* v_rows, const int32_t* row_seq, const int32_t* row_pos, uint32_t n_rows,
+                               const int32_t* block_table, uint32_t table_stride, uint32_t n_seq, int32_t* err,
+                               pa_stream_t stream) {
   pa_pool_desc d;
   if (pa_pool_get_desc(pool, &d) != PA_OK) return PA_ERR_INVALID;
   if (n_rows == 0) return PA_OK;
@@ -132,6 +217,7 @@ extern "C" pa_status pa_append_rows(const pa_pool* pool, void* k_pool, void* v_p
   const size_t rbk = pa_row_bytes(d.k_type, d.head_dim), rbv = pa_row_bytes(d.v_type, d.head_dim);
   if (rbk == 0 || rbv == 0) return PA_ERR_UNSUPPORTED;
   if ((rbk | rbv) & 15) return PA_ERR_UNSUPPORTED;  // every supported format is a multiple of 16
+  if (d.head_dim != (uint32_t)kD_append) return PA_ERR_UNSUPPORTED;
   if (((uintptr_t)k_pool | (uintptr_t)v_pool | (uintptr_t)k_rows | (uintptr_t)v_rows) & 15) return PA_ERR_INVALID;
   AppendParams p{};
   p.k_pool = static_cast<uint8_t*>(k_pool);
@@ -150,8 +236,9 @@ extern "C" pa_status pa_append_rows(const pa_pool* pool, void* k_pool, void* v_p
   p.n_blocks = (int)d.n_blocks;
   p.k_type = (int)d.k_type;
   p.v_type = (int)d.v_type;
-  p.k_units = d.k_type == PA_F16 ? (int)(rbk / 16) : (int)(d.head_dim / 32);
-  p.v_units = d.v_type == PA_F16 ? (int)(rbv / 16) : (int)(d.head_dim / 32);
+  const int blocks = (int)(d.head_dim / 32);
+  p.k_units = (!f16_in && d.k_type == PA_F16) ? (int)(rbk / 16) : blocks;
+  p.v_units = (!f16_in && d.v_type == PA_F16) ? (int)(rbv / 16) : blocks;
   p.k_row = (int)rbk;
   p.v_row = (int)rbv;
   const long long total = (long long)n_rows * d.n_kv_heads * (p.k_units + p.v_units);
@@ -160,8 +247,29 @@ extern "C" pa_status pa_append_rows(const pa_pool* pool, void* k_pool, void* v_p
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return PA_ERR_CUDA;
   const long long want = (total + 255) / 256;
   const int grid = (int)(want < (long long)sms * 16 ? want : (long long)sms * 16);
-  pa_append_kernel<<<grid, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (f16_in) {
+    pa_append_kernel<true><<<grid, 256, 0, cs>>>(p);
+  } else {
+    pa_append_kernel<false><<<grid, 256, 0, cs>>>(p);
+  }
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+extern "C" pa_status pa_append_rows(const pa_pool* pool, void* k_pool, void* v_pool, const void* k_rows,
+                                    const void* v_rows, const int32_t* row_seq, const int32_t* row_pos,
+                                    uint32_t n_rows, const int32_t* block_table, uint32_t table_stride,
+                                    uint32_t n_seq, int32_t* err, pa_stream_t stream) {
+  return launch_append(false, pool, k_pool, v_pool, k_rows, v_rows, row_seq, row_pos, n_rows, block_table,
+                       table_stride, n_seq, err, stream);
+}
+
+extern "C" pa_status pa_append_rows_f16(const pa_pool* pool, void* k_pool, void* v_pool, const uint16_t* k_rows,
+                                        const uint16_t* v_rows, const int32_t* row_seq, const int32_t* row_pos,
+                                        uint32_t n_rows, const int32_t* block_table, uint32_t table_stride,
+                                        uint32_t n_seq, int32_t* err, pa_stream_t stream) {
+  return launch_append(true, pool, k_pool, v_pool, k_rows, v_rows, row_seq, row_pos, n_rows, block_table,
+                       table_stride, n_seq, err, stream);
 }
 
 extern "C" pa_status pa_get_error(int32_t* err, pa_stream_t stream) {

@@ -74,3 +74,72 @@ def test_append_bounds_guard():
     oracle.scatter(vo2, w.n_blocks, 4, 16, w.v_type, oracle.ROLE_V, w.v_rows[keep], w.row_seq[keep], w.row_pos[keep], good)
     assert np.array_equal(c.k_pool.cpu().numpy(), ko2)
     assert np.array_equal(c.v_pool.cpu().numpy(), vo2)
+
+
+# ------------------------------------------------------------------ quantise on append
+
+def _rows_f16(rng, n):
+    """binary16 sources [n][4][256] with planted edge blocks: all zero, ties in
+    magnitude, products that land exactly on .5 (d = 1 blocks), tiny values."""
+    x = rng.standard_normal((n, 4, 256)).astype(np.float32)
+    x[0, 0, :32] = 0.0
+    x[0, 1, :32] = np.linspace(-2, 2, 32)          # -2 and +2: a tie in magnitude
+    x[1, 2, :32] = 0.0
+    x[1, 2, 0] = 127.0                             # Q8_0 d = 1: q = x exactly
+    x[1, 2, 1:9] = [2.5, -2.5, 0.5, -0.5, 1.5, -1.5, 126.5, -126.5]
+    x[1, 3, :32] = 0.0
+    x[1, 3, 0] = -8.0                              # Q4_0 d = 1
+    x[1, 3, 1:9] = [-7.5, 6.5, 7.0, 7.5, -0.5, 0.5, 0.25, -8.0]
+    x[2, 0, :32] *= 1e-5                           # scales in the fp16 subnormal range
+    return x.astype(np.float16).view(np.uint16)
+
+
+QCASES = [("q4_0", W.TYPE_Q4_0, W.TYPE_Q4_0), ("q8_0", W.TYPE_Q8_0, W.TYPE_Q8_0),
+          ("f16", W.TYPE_F16, W.TYPE_F16), ("q8k-q4v", W.TYPE_Q8_0, W.TYPE_Q4_0)]
+
+
+@pytest.mark.parametrize("name,kt,vt", QCASES, ids=[c[0] for c in QCASES])
+def test_quantise_on_append_matches_oracle(name, kt, vt):
+    """fp16 rows quantised by the append kernel give, byte for byte, the pools
+    of the oracle's quantiser followed by the oracle's scatter."""
+    w = W.make_workload(name, 60, [100, 33, 16, 48], 16, kt, vt, 1, "shuffled")
+    rng = np.random.default_rng(61)
+    n = int(w.row_seq.shape[0])
+    hk, hv = _rows_f16(rng, n), _rows_f16(rng, n)
+    ref = W.Workload(name, w.seq_lens, 1, w.page_size, w.n_blocks, kt, vt, w.table,
+                     oracle.quantize_rows(hk, kt), oracle.quantize_rows(hv, vt), w.q)
+    ko, vo = oracle_pools(ref)
+    c = PagedKVCache(w.n_blocks, w.page_size, kt, vt)
+    c.append_f16(to_dev(hk), to_dev(hv), to_dev(w.row_seq), to_dev(w.row_pos), to_dev(w.table))
+    assert c.check() == PA_OK
+    assert np.array_equal(c.k_pool.cpu().numpy(), ko)
+    assert np.array_equal(c.v_pool.cpu().numpy(), vo)
+
+
+def test_quantise_on_append_large_sampled():
+    """The many-sequence workload's shape (64 sequences, lognormal lengths,
+    Q8_0 K with Q4_0 V) quantised on append; sampled rows against the oracle's
+    quantiser, read back through the documented pool layout."""
+    base = W.config(5, variant="b")
+    rng = np.random.default_rng(62)
+    n = int(base.row_seq.shape[0])
+    hk = rng.standard_normal((n, 4, 256)).astype(np.float16).view(np.uint16)
+    hv = rng.standard_normal((n, 4, 256)).astype(np.float16).view(np.uint16)
+    kt, vt = W.TYPE_Q8_0, W.TYPE_Q4_0
+    c = PagedKVCache(base.n_blocks, base.page_size, kt, vt)
+    c.append_f16(to_dev(hk), to_dev(hv), to_dev(base.row_seq), to_dev(base.row_pos), to_dev(base.table))
+    assert c.check() == PA_OK
+    kp, vp = c.k_pool.cpu().numpy(), c.v_pool.cpu().numpy()
+    pick = rng.choice(n, 64, replace=False)
+    for t, role, pool, src in ((kt, oracle.ROLE_K, kp, hk), (vt, oracle.ROLE_V, vp, hv)):
+        rb = oracle.row_bytes(t)
+        offs = np.array([[oracle.group_offset(t, role, r, i) for i in range(rb)] for r in range(16)])
+        want = oracle.quantize_rows(src[pick], t)
+        for k, i in enumerate(pick):
+            s, pos = int(base.row_seq[i]), int(base.row_pos[i])
+            blk = int(base.table[s, pos // base.page_size])
+            slot = pos % base.page_size
+            for h in range(4):
+                grp = ((blk * 4 + h) * base.page_size + slot // 16 * 16) * rb
+                got = pool[grp + offs[slot % 16]]
+                assert np.array_equal(got, want[k, h]), (t, i, h)

@@ -342,6 +342,88 @@ def pin_fully_masked_part():
     assert lse == -np.inf and np.array_equal(out, np.zeros(D))
 
 
+# ------------------------------------------------------------------ quantise on append
+
+def pin_float_to_half_vs_numpy():
+    """fp32 -> fp16 rounding (nearest, ties to even) against numpy's own
+    binary16 conversion: random values over the whole range, exact ties,
+    subnormals, overflow and signed zeros."""
+    rng = np.random.default_rng(17)
+    parts = [rng.standard_normal(4000).astype(np.float32) * np.float32(2.0) ** rng.integers(-30, 18, 4000)]
+    # exact halfway points between neighbouring binary16 values (ties)
+    h = rng.integers(0, 0x7bff, 2000).astype(np.uint16)
+    a = h.view(np.float16).astype(np.float32)
+    b = (h + 1).astype(np.uint16).view(np.float16).astype(np.float32)
+    parts.append(((a.astype(np.float64) + b.astype(np.float64)) / 2).astype(np.float32))
+    parts.append(np.array([0.0, -0.0, 65504, 65519.99, 65520, 1e9, -1e9, 2.0 ** -24, 2.0 ** -25,
+                           1.5 * 2.0 ** -25, 2.0 ** -26, 6.1e-5, 6.097e-5], np.float32))
+    x = np.concatenate(parts)
+    with np.errstate(over="ignore"):
+        ref = x.astype(np.float16).view(np.uint16)
+    assert np.array_equal(oracle.float_to_half(x), ref)
+
+
+def _h(vals):
+    return np.asarray(vals, np.float32).astype(np.float16).view(np.uint16)
+
+
+def pin_quantiser_closed_forms():
+    """Blocks whose quantisation is known in closed form."""
+    # Q8_0: x = k/8, amax = 127/8 -> d = 1/8 exactly, q = k exactly
+    k = np.arange(-127, 128, 8)[:32].astype(np.float32)
+    k[0] = -127
+    out = oracle.quantize_rows(_h(k / 8), W.TYPE_Q8_0)
+    assert out[0] == 0x00 and out[1] == 0x30  # fp16(0.125)
+    assert np.array_equal(out[2:].view(np.int8), k.astype(np.int8))
+    # Q8_0 rounds half away from zero: d = 1, x = +-2.5 -> +-3, +-0.5 -> +-1
+    x = np.zeros(32, np.float32)
+    x[:5] = [127, 2.5, -2.5, 0.5, -0.5]
+    q = oracle.quantize_rows(_h(x), W.TYPE_Q8_0)[2:].view(np.int8)
+    assert list(q[:5]) == [127, 3, -3, 1, -1] and not q[5:].any()
+    # Q4_0: largest magnitude -2 (first on ties) -> d = 0.25; x = (q - 8) / 4 -> q
+    qs = np.arange(32) % 16
+    x = (qs - 8) / 4.0
+    x[1], x[17] = -2.0, 2.0  # a tie in magnitude: the first (-2) sets d = +0.25; +2 clamps to 15
+    out = oracle.quantize_rows(_h(x), W.TYPE_Q4_0)
+    assert out[0] == 0x00 and out[1] == 0x34  # fp16(0.25)
+    nib = np.concatenate([out[2:] & 15, out[2:] >> 4])
+    want = qs.copy()
+    want[1], want[17] = 0, 15
+    assert np.array_equal(nib, want)
+    # Q4_0 with a positive extreme: d = -m/8 < 0, the extreme maps to q = 0
+    x = np.zeros(32, np.float32)
+    x[3] = 4.0
+    out = oracle.quantize_rows(_h(x), W.TYPE_Q4_0)
+    assert out[0] == 0x00 and out[1] == 0xb8  # fp16(-0.5)
+    nib = np.concatenate([out[2:] & 15, out[2:] >> 4])
+    assert nib[3] == 0 and (np.delete(nib, 3) == 8).all()
+    # all-zero blocks
+    z = np.zeros(32, np.uint16)
+    assert np.array_equal(oracle.quantize_rows(z, W.TYPE_Q8_0), np.zeros(34, np.uint8))
+    zq4 = oracle.quantize_rows(z, W.TYPE_Q4_0)
+    assert zq4[1] == 0x80 and zq4[0] == 0 and (zq4[2:] == 0x88).all()  # d = 0 / -8 = -0.0
+    # F16 is a copy
+    r = np.random.default_rng(3).integers(0, 0x7c00, 256).astype(np.uint16)
+    assert np.array_equal(oracle.quantize_rows(r, W.TYPE_F16).view(np.uint16), r)
+
+
+def pin_quantiser_error_bounds():
+    """Dequantised values lie within half a step (Q8_0) or one step (Q4_0) of
+    the input, plus what storing the scale in fp16 adds (|q| <= 128 times a
+    relative 2^-11 of the step: 1/16 of a step), most within half a step."""
+    rng = np.random.default_rng(21)
+    x = rng.standard_normal((64, 256)).astype(np.float32)
+    h = _h(x)
+    xf = h.view(np.float16).astype(np.float64)
+    for t, steps, bound in ((W.TYPE_Q8_0, 127.0, 0.5), (W.TYPE_Q4_0, 8.0, 1.0)):
+        deq = oracle.dequant_rows(oracle.quantize_rows(h, t), t)
+        amax = np.abs(xf.reshape(-1, 32)).max(axis=1)
+        step = (amax / steps).repeat(32).reshape(xf.shape)
+        err = np.abs(deq - xf)
+        assert (err <= (bound + 1 / 16) * step + 1e-12).all(), t
+        assert (err <= 0.5 * step * (1 + 1e-3) + 1e-12).mean() > 0.97, t
+
+
 # ------------------------------------------------------------------ pool layout
 
 # Offsets worked out by hand from the written layout definition (pa.h, "Pool
@@ -393,7 +475,8 @@ PINS = [pin_half_all_patterns, pin_q8_0_hand_block, pin_q4_0_hand_block,
         pin_subnormal_and_negative_scales, pin_capacity_table, pin_rdna4_bandwidth,
         pin_quantiser_roundtrip, pin_one_key, pin_identical_keys_and_zero_query, pin_gqa_mapping,
         pin_causal_verify, pin_dominant_key, pin_dense_brute_force,
-        pin_placement_and_page_size_invariance, pin_split_merge, pin_fully_masked_part, pin_group_layout]
+        pin_placement_and_page_size_invariance, pin_split_merge, pin_fully_masked_part, pin_group_layout,
+        pin_float_to_half_vs_numpy, pin_quantiser_closed_forms, pin_quantiser_error_bounds]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -428,6 +511,10 @@ MUTATIONS = [
      "const uint8_t* grp = pool + ((blk * (long)c->page_size + slot / ORC_GROUP * ORC_GROUP) * c->hkv + g) * rb;"),
     ("layout_no_swizzle", "return 32L * nb + (r * chunks + (c ^ (r % 8))) * 16 + qi % 16;",
      "return 32L * nb + (r * chunks + c) * 16 + qi % 16;"),
+    ("quant_round_even", "out[2 + i] = (uint8_t)(int8_t)roundf(v);", "out[2 + i] = (uint8_t)(int8_t)rintf(v);"),
+    ("quant_q4_sign", "const float d = m / -8.0f;", "const float d = m / 8.0f;"),
+    ("quant_q4_no_clamp", "q[i] = t < 15 ? t : 15;", "q[i] = t;"),
+    ("half_round_up", "if (rem > half || (rem == half && (q & 1u))) ++q;", "if (rem >= half) ++q;"),
     ("v_scale_pairs", "8 * (b % 2) + 4 * (r / 8) + 2 * (r % 2) + o;", "4 * (b % 2) + 8 * (r / 8) + 2 * (r % 2) + o;"),
     ("softmax_sign", "double w = exp(z[j - j0] - m);", "double w = exp(m - z[j - j0]);"),
     ("lse_drops_max", "lse[base] = (l > 0.0) ? m + log(l) : -INFINITY;",
