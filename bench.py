@@ -62,6 +62,8 @@ def workload_for(name: str) -> W.Workload:
         return W.config(5, variant="a")
     if name == "many":
         return W.config(5, variant="b")
+    if name == "shared-prefix":  # 8 sequences forked from a 32K-token prompt, 1K own rows each
+        return W.shared_prefix()
     if name.startswith("percall-"):  # percall-<32k|131k|262k>-<1|3|4>: Q8_0 K / Q4_0 V, one sequence
         _, size, nq = name.split("-")
         return W.percall({"32k": 32768, "131k": 131072, "262k": 262144}[size], int(nq))

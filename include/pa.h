@@ -130,6 +130,41 @@ pa_status pa_block_index(const pa_pool* pool, pa_block handle, int32_t* idx);
 /* Number of free blocks. */
 uint32_t pa_pool_free_count(const pa_pool* pool);
 
+/* ------------------------------------------------------------------ prefix sharing
+ * Prefix blocks shared between sequences by reference count, with
+ * copy-on-write (lucebox PR #555, roadmap item 6).  A block holds one
+ * reference after pa_alloc_blocks; pa_release drops one reference per
+ * occurrence of a handle and frees the block (bumping its generation) when
+ * the count reaches 0, so a handle may occur in one pa_release call as many
+ * times as it has references (more is PA_ERR_STALE, nothing released).
+ * Thread-safe; every call checks everything before it commits. */
+
+/* Take one more reference per occurrence of each handle (a sequence that
+ * forks another puts the same blocks in its own table).  PA_ERR_STALE for a
+ * handle that is not live: nothing changes. */
+pa_status pa_share_blocks(pa_pool* pool, const pa_block* handles, uint32_t n);
+
+/* Reference count of a live block (PA_ERR_STALE otherwise). */
+pa_status pa_block_refcount(const pa_pool* pool, pa_block handle, uint32_t* count);
+
+/* Prepare blocks for writing.  Taking the handles in order, a block held by
+ * one reference comes back unchanged in out[i]; a shared block loses the
+ * caller's reference and out[i] is a freshly allocated block, with the pair
+ * (old index, new index) appended to copy_src / copy_dst (host arrays of
+ * capacity n; *n_copies pairs written).  The caller then copies the listed
+ * blocks on the device (pa_copy_blocks) before writing to them, and puts
+ * out[i] in its table.  PA_ERR_STALE (a handle not live) or PA_ERR_OOM (too
+ * few free blocks for the copies): nothing changes. */
+pa_status pa_cow_blocks(pa_pool* pool, const pa_block* handles, uint32_t n, pa_block* out,
+                        int32_t* copy_src, int32_t* copy_dst, uint32_t* n_copies);
+
+/* Device half of copy-on-write: copy whole blocks (every KV head's page of K
+ * and of V) from block src[i] to block dst[i], i < n.  src, dst: device int32
+ * arrays.  A pair with an index outside the pool is skipped and sets
+ * *err = PA_ERR_BOUNDS.  Pairs that write one block twice race. */
+pa_status pa_copy_blocks(const pa_pool* pool, void* k_pool, void* v_pool, const int32_t* src,
+                         const int32_t* dst, uint32_t n, int32_t* err, pa_stream_t stream);
+
 /* ------------------------------------------------------------------ append
  * New rows are uploaded once, packed, and a kernel scatters them into their
  * page slots (colibri PR #372, Summary: one packed transfer of the newly

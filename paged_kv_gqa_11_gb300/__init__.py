@@ -18,7 +18,7 @@ import threading
 from . import _build
 
 __all__ = [
-    "PA_F16", "PA_Q4_0", "PA_Q8_0", "PaError", "Pool", "load", "row_bytes", "pa_append_rows", "pa_append_rows_f16", "pa_decode",
+    "PA_F16", "PA_Q4_0", "PA_Q8_0", "PaError", "Pool", "load", "row_bytes", "pa_append_rows", "pa_append_rows_f16", "pa_copy_blocks", "pa_decode",
     "pa_decode_workspace_size", "pa_decode_plan", "pa_get_error", "pa_selftest_wait_timeout", "status_name",
     "library_path", "pa_decode_noalloc",
 ]
@@ -30,7 +30,8 @@ PA_OK, PA_ERR_INVALID, PA_ERR_UNSUPPORTED, PA_ERR_OOM, PA_ERR_STALE, PA_ERR_BOUN
 
 # Every entry point declared in include/pa.h.
 EXPORTS = ["pa_pool_create", "pa_pool_destroy", "pa_pool_get_desc", "pa_row_bytes", "pa_pool_bytes",
-           "pa_alloc_blocks", "pa_release", "pa_block_index", "pa_pool_free_count", "pa_append_rows", "pa_append_rows_f16",
+           "pa_alloc_blocks", "pa_release", "pa_block_index", "pa_pool_free_count", "pa_share_blocks", "pa_block_refcount",
+           "pa_cow_blocks", "pa_copy_blocks", "pa_append_rows", "pa_append_rows_f16",
            "pa_decode", "pa_decode_split", "pa_decode_merge", "pa_decode_workspace_size", "pa_decode_plan", "pa_get_error", "pa_status_string",
            "pa_selftest_wait_timeout", "pa_decode_noalloc"]
 
@@ -79,6 +80,10 @@ def load():
             "pa_release": (C.c_int, [vp, vp, u32]),
             "pa_block_index": (C.c_int, [vp, C.c_uint64, C.POINTER(i32)]),
             "pa_pool_free_count": (u32, [vp]),
+            "pa_share_blocks": (C.c_int, [vp, vp, u32]),
+            "pa_block_refcount": (C.c_int, [vp, C.c_uint64, C.POINTER(u32)]),
+            "pa_cow_blocks": (C.c_int, [vp, vp, u32, vp, vp, vp, C.POINTER(u32)]),
+            "pa_copy_blocks": (C.c_int, [vp, vp, vp, vp, vp, u32, vp, vp]),
             "pa_append_rows": (C.c_int, [vp, vp, vp, vp, vp, vp, vp, u32, vp, u32, u32, vp, vp]),
             "pa_append_rows_f16": (C.c_int, [vp, vp, vp, vp, vp, vp, vp, u32, vp, u32, u32, vp, vp]),
             "pa_decode": (C.c_int, [vp, vp, vp, vp, vp, u32, vp, vp, u32, u32, u32, C.c_float, vp, vp, vp, sz,
@@ -184,6 +189,27 @@ class Pool:
     def free_count(self) -> int:
         return int(load().pa_pool_free_count(self._h))
 
+    def share(self, handles) -> int:
+        arr = (C.c_uint64 * max(len(handles), 1))(*handles)
+        return int(load().pa_share_blocks(self._h, arr, len(handles)))
+
+    def refcount(self, handle: int):
+        n = C.c_uint32(0)
+        rc = load().pa_block_refcount(self._h, handle, C.byref(n))
+        return rc, n.value
+
+    def cow(self, handles):
+        """Returns (status, handles to write through, [(src index, dst index)] copies)."""
+        k = max(len(handles), 1)
+        arr = (C.c_uint64 * k)(*handles)
+        out = (C.c_uint64 * k)()
+        src, dst = (C.c_int32 * k)(), (C.c_int32 * k)()
+        nc = C.c_uint32(0)
+        rc = int(load().pa_cow_blocks(self._h, arr, len(handles), out, src, dst, C.byref(nc)))
+        if rc != PA_OK:
+            return rc, [], []
+        return rc, list(out[:len(handles)]), [(src[i], dst[i]) for i in range(nc.value)]
+
 
 def pa_append_rows(pool: Pool, k_pool, v_pool, k_rows, v_rows, row_seq, row_pos, n_rows: int, block_table,
                    table_stride: int, n_seq: int, err, stream=None) -> None:
@@ -200,6 +226,13 @@ def pa_append_rows_f16(pool: Pool, k_pool, v_pool, k_rows, v_rows, row_seq, row_
                                    _ptr(row_seq), _ptr(row_pos), n_rows, _ptr(block_table), table_stride, n_seq,
                                    _ptr(err), _stream(stream))
     _check(rc, "pa_append_rows_f16")
+
+
+def pa_copy_blocks(pool: Pool, k_pool, v_pool, src, dst, n: int, err, stream=None) -> None:
+    """Copy whole blocks src[i] -> dst[i] (device int32 arrays) in both pools."""
+    rc = load().pa_copy_blocks(pool.handle, _ptr(k_pool), _ptr(v_pool), _ptr(src), _ptr(dst), n, _ptr(err),
+                               _stream(stream))
+    _check(rc, "pa_copy_blocks")
 
 
 def pa_decode_workspace_size(pool: Pool, n_seq: int, n_qtok: int, device: int = 0) -> int:

@@ -187,6 +187,42 @@ __global__ void __launch_bounds__(256) pa_append_kernel(const __grid_constant__ 
   }
 }
 
+// Copy-on-write, device half: whole blocks (every KV head's page, K and V)
+// from src[i] to dst[i], 16 bytes per thread.  A pair with an index outside
+// the pool is skipped and reported.
+struct CopyParams {
+  uint8_t* k_pool;
+  uint8_t* v_pool;
+  const int32_t* src;
+  const int32_t* dst;
+  int32_t* err;
+  long long n;
+  long long k_chunks, v_chunks;  // 16-byte chunks per block
+  int n_blocks;
+};
+
+__global__ void __launch_bounds__(256) pa_copy_blocks_kernel(const __grid_constant__ CopyParams p) {
+  const long long per = p.k_chunks + p.v_chunks;
+  const long long total = p.n * per;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+    const long long pair = i / per, c = i - pair * per;
+    const int s = __ldg(p.src + pair), d = __ldg(p.dst + pair);
+    if (s < 0 || s >= p.n_blocks || d < 0 || d >= p.n_blocks) {
+      if (c == 0) record_error(p.err, PA_ERR_BOUNDS);
+      continue;
+    }
+    if (c < p.k_chunks) {
+      const uint4* from = reinterpret_cast<const uint4*>(p.k_pool) + s * p.k_chunks + c;
+      reinterpret_cast<uint4*>(p.k_pool)[d * p.k_chunks + c] = *from;
+    } else {
+      const long long cv = c - p.k_chunks;
+      const uint4* from = reinterpret_cast<const uint4*>(p.v_pool) + s * p.v_chunks + cv;
+      reinterpret_cast<uint4*>(p.v_pool)[d * p.v_chunks + cv] = *from;
+    }
+  }
+}
+
 __global__ void pa_wait_selftest_kernel(uint64_t limit_ns, int32_t* err) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ int abort_flag;
@@ -270,6 +306,35 @@ extern "C" pa_status pa_append_rows_f16(const pa_pool* pool, void* k_pool, void*
                                         uint32_t n_seq, int32_t* err, pa_stream_t stream) {
   return launch_append(true, pool, k_pool, v_pool, k_rows, v_rows, row_seq, row_pos, n_rows, block_table,
                        table_stride, n_seq, err, stream);
+}
+
+extern "C" pa_status pa_copy_blocks(const pa_pool* pool, void* k_pool, void* v_pool, const int32_t* src,
+                                    const int32_t* dst, uint32_t n, int32_t* err, pa_stream_t stream) {
+  pa_pool_desc d;
+  if (pa_pool_get_desc(pool, &d) != PA_OK) return PA_ERR_INVALID;
+  if (n == 0) return PA_OK;
+  if (!k_pool || !v_pool || !src || !dst || !err) return PA_ERR_INVALID;
+  if (((uintptr_t)k_pool | (uintptr_t)v_pool) & 15) return PA_ERR_INVALID;
+  const size_t bk = (size_t)d.n_kv_heads * d.page_size * pa_row_bytes(d.k_type, d.head_dim);
+  const size_t bv = (size_t)d.n_kv_heads * d.page_size * pa_row_bytes(d.v_type, d.head_dim);
+  if (bk == 0 || bv == 0 || ((bk | bv) & 15)) return PA_ERR_UNSUPPORTED;
+  CopyParams p{};
+  p.k_pool = static_cast<uint8_t*>(k_pool);
+  p.v_pool = static_cast<uint8_t*>(v_pool);
+  p.src = src;
+  p.dst = dst;
+  p.err = err;
+  p.n = n;
+  p.k_chunks = (long long)(bk / 16);
+  p.v_chunks = (long long)(bv / 16);
+  p.n_blocks = (int)d.n_blocks;
+  int device = 0, sms = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return PA_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return PA_ERR_CUDA;
+  const long long want = ((long long)n * (p.k_chunks + p.v_chunks) + 255) / 256;
+  const int grid = (int)(want < (long long)sms * 16 ? want : (long long)sms * 16);
+  pa_copy_blocks_kernel<<<grid, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 extern "C" pa_status pa_get_error(int32_t* err, pa_stream_t stream) {

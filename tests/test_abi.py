@@ -86,10 +86,31 @@ def _random_ops(seed, n_blocks, steps):
                 s = set(idx.tolist())
                 stale += [h for i, h in enumerate(held) if i in s]
                 held = [h for i, h in enumerate(held) if i not in s]
+        elif r < 0.86 and held:  # share some held blocks (each share is one more reference to drop)
+            k = int(rng.integers(1, min(len(held), 4) + 1))
+            sh = [held[int(i)] for i in rng.choice(len(held), size=k)]
+            if rng.random() < 0.2 and stale:
+                sh.append(stale[-1])
+            rc = lib_pool.share(sh)
+            assert rc == model.share(sh)
+            if rc == pa.PA_OK:
+                held += sh
+        elif r < 0.93 and held:  # copy-on-write of some held references
+            k = int(rng.integers(1, min(len(held), 5) + 1))
+            idx = sorted(rng.choice(len(held), size=k, replace=False).tolist())
+            cw = [held[i] for i in idx]
+            if rng.random() < 0.1 and stale:
+                cw.append(stale[-1])
+            got = lib_pool.cow(cw)
+            assert got == model.cow(cw)
+            if got[0] == pa.PA_OK:
+                for i, h in zip(idx, got[1]):
+                    held[i] = h
         else:
             probe = held + stale[-5:] + [(7 << 32) | (n_blocks + 3)]
             for h in probe:
                 assert lib_pool.block_index(h) == model.block_index(h)
+                assert lib_pool.refcount(h) == model.refcount(h)
         assert lib_pool.free_count() == model.free_count()
 
 
@@ -109,6 +130,25 @@ def test_allocator_oom_and_stale(lib):
     assert p.block_index(hs[1]) == (pa.PA_OK, 1)
     again = p.alloc(1)[0]
     assert again & 0xFFFFFFFF == 0 and again >> 32 == 2      # immediate reuse, new generation
+
+
+def test_share_release_and_cow(lib):
+    """Shared blocks stay live until every reference is dropped; cow swaps a
+    shared block for a fresh one and lists the copy."""
+    p = pa.Pool(4, 16, 4, 256, pa.PA_F16)
+    a, b = p.alloc(2)
+    assert p.share([a, a]) == pa.PA_OK and p.refcount(a) == (pa.PA_OK, 3)
+    rc, out, copies = p.cow([a, b])
+    assert rc == pa.PA_OK and out[1] == b and out[0] != a and copies == [(0, 2)]
+    assert p.refcount(a) == (pa.PA_OK, 2) and p.refcount(out[0]) == (pa.PA_OK, 1)
+    assert p.release([a, a, a]) == pa.PA_ERR_STALE and p.refcount(a) == (pa.PA_OK, 2)  # more than held
+    assert p.release([a, a]) == pa.PA_OK and p.block_index(a)[0] == pa.PA_ERR_STALE
+    assert p.alloc(1)[0] == (2 << 32) | 0  # freed at the last reference, new generation
+    # not enough free blocks for the copies: nothing changes
+    q = pa.Pool(2, 16, 4, 256, pa.PA_F16)
+    x, y = q.alloc(2)
+    q.share([x, y])
+    assert q.cow([x, y])[0] == pa.PA_ERR_OOM and q.refcount(x) == (pa.PA_OK, 2) and q.free_count() == 0
 
 
 def test_decode_rejects_unsupported_shapes_on_host(lib):

@@ -7,7 +7,7 @@ from oracle.allocator_model import OK, OOM, STALE, AllocatorModel
 
 
 def _state(a):
-    return (list(a.gen), list(a.live), list(a.stack))
+    return (list(a.gen), list(a.ref), list(a.stack))
 
 
 def test_fresh_pool_hands_out_blocks_in_order():
@@ -73,3 +73,34 @@ def test_random_sequences_keep_invariants():
             assert len(set(live_idx)) == len(live_idx)
             assert a.free_count() + len(held) == n
             assert all(a.block_index(h)[0] == OK for h in held)
+
+
+def test_shared_blocks_free_at_last_reference():
+    """A shared block is freed (and its generation bumped) only when its last
+    reference is released; releasing more references than held changes
+    nothing."""
+    a = AllocatorModel(3)
+    _, (h,) = a.alloc(1)
+    assert a.share([h, h]) == OK and a.refcount(h) == (OK, 3)
+    before = _state(a)
+    assert a.release([h, h, h, h]) == STALE and _state(a) == before
+    assert a.release([h]) == OK and a.refcount(h) == (OK, 2) and a.free_count() == 2
+    assert a.release([h, h]) == OK and a.refcount(h) == (STALE, 0) and a.free_count() == 3
+    assert a.alloc(1) == (OK, [AllocatorModel.handle(2, 0)])
+
+
+def test_cow_copies_only_shared_blocks_and_is_all_or_nothing():
+    a = AllocatorModel(4)
+    _, (x, y) = a.alloc(2)
+    a.share([x])
+    rc, out, pairs = a.cow([x, y, x])
+    # x shared twice: the first occurrence copies (x keeps one reference), the
+    # second finds it held once and keeps it; y is private
+    assert rc == OK and out[1] == y and out[2] == x and pairs == [(0, 2)]
+    assert a.refcount(x) == (OK, 1) and a.refcount(out[0]) == (OK, 1)
+    b = AllocatorModel(2)
+    _, (u, v) = b.alloc(2)
+    b.share([u, v])
+    before = _state(b)
+    assert b.cow([u, v])[0] == OOM and _state(b) == before
+    assert b.cow([u, (9 << 32) | 1])[0] == STALE and _state(b) == before

@@ -12,6 +12,7 @@ import workloads as W
 from gpu_helpers import assert_close, assert_lse_close, device_cache, run_decode, to_dev
 from paged_kv_gqa_11_gb300 import (PA_ERR_BOUNDS, PA_ERR_TIMEOUT, PA_OK, _build, pa_decode_plan,
                                    pa_selftest_wait_timeout)
+from paged_kv_gqa_11_gb300.cache import PagedKVCache
 
 pytestmark = pytest.mark.gpu
 THREADS = os.cpu_count() or 1
@@ -238,7 +239,6 @@ def test_plan_covers_every_tile():
     """One query token: 16-key tiles of all four KV heads (one segment per
     sequence); more tokens: 64-key tiles of one head (four per sequence)."""
     w = W.config(3)
-    from paged_kv_gqa_11_gb300.cache import PagedKVCache
     c = PagedKVCache(w.n_blocks, w.page_size, w.k_type, w.v_type)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     for nq, keys, segs in ((1, 16, 1), (2, 64, W.HKV)):
@@ -248,3 +248,78 @@ def test_plan_covers_every_tile():
         assert 0 < plan["ctas"] <= tiles
         assert plan["ctas"] % sms == 0 or plan["ctas"] == tiles
         assert plan["partials"] >= w.n_seq * segs
+
+
+def test_prefix_fork_with_copy_on_write():
+    """Sequence A (100 rows) is forked into B by sharing its blocks.  B's
+    partly filled last page is copied on write before B appends 20 rows; A
+    then appends 10 other rows into its own, now unshared, last page.  Both
+    decode like the oracle on their logical rows, and the copy is byte-exact."""
+    from paged_kv_gqa_11_gb300 import pa_copy_blocks
+    ps, kt, vt = 16, Q8, Q4
+    rng = np.random.default_rng(91)
+    c = PagedKVCache(32, ps, kt, vt)
+    pool = c.pool
+    rows_k = W.random_rows(rng, 130, kt)
+    rows_v = W.random_rows(rng, 130, vt)
+    a_pre, a_new, b_new = slice(0, 100), slice(100, 110), slice(110, 130)
+    hA = pool.alloc(7)
+    tA = [pool.block_index(h)[1] for h in hA]
+
+    def put(table_row, k, v, positions):
+        n = len(positions)
+        tab = to_dev(np.array([table_row + [-1] * (8 - len(table_row))], np.int32))
+        c.append(to_dev(k), to_dev(v), to_dev(np.zeros(n, np.int32)), to_dev(np.array(positions, np.int32)), tab)
+        assert c.check() == PA_OK
+
+    put(tA, rows_k[a_pre], rows_v[a_pre], list(range(100)))
+    # fork: B shares A's blocks
+    assert pool.share(hA) == PA_OK and pool.refcount(hA[6]) == (PA_OK, 2)
+    rc, (hB6,), copies = pool.cow([hA[6]])
+    assert rc == PA_OK and len(copies) == 1 and copies[0][0] == tA[6]
+    pa_copy_blocks(pool, c.k_pool, c.v_pool, to_dev(np.array([copies[0][0]], np.int32)),
+                   to_dev(np.array([copies[0][1]], np.int32)), 1, c.err)
+    assert c.check() == PA_OK
+    kb = c.k_pool.view(32, -1)
+    vb = c.v_pool.view(32, -1)
+    assert torch.equal(kb[copies[0][1]], kb[tA[6]]) and torch.equal(vb[copies[0][1]], vb[tA[6]])
+    hB7 = pool.alloc(1)[0]
+    tB = tA[:6] + [copies[0][1], pool.block_index(hB7)[1]]
+    put(tB, rows_k[b_new], rows_v[b_new], list(range(100, 120)))
+    # A's last page is now held once: cow keeps it
+    rc, (hA6,), none = pool.cow([hA[6]])
+    assert rc == PA_OK and hA6 == hA[6] and none == []
+    put(tA, rows_k[a_new], rows_v[a_new], list(range(100, 110)))
+    table = np.full((2, 8), -1, np.int32)
+    table[0, :7] = tA
+    table[1, :8] = tB
+    lens = np.array([110, 120], np.int32)
+    q = rng.standard_normal((2, 1, W.HQ, W.D), dtype=np.float32)
+    out, lse = c.decode(to_dev(q), to_dev(table), to_dev(lens), lens, 1)
+    c.raise_on_error()
+    # the oracle sees each sequence's logical rows through its own private layout
+    ref = W.Workload("fork", lens, 1, ps, 15, kt, vt,
+                     W.table_from_lists([list(range(7)), list(range(7, 15))]),
+                     np.concatenate([rows_k[a_pre], rows_k[a_new], rows_k[a_pre], rows_k[b_new]]),
+                     np.concatenate([rows_v[a_pre], rows_v[a_new], rows_v[a_pre], rows_v[b_new]]), q)
+    oo, ol = oracle.decode_workload(ref, n_threads=THREADS)
+    assert_close(out.cpu().numpy(), oo, what="fork")
+    assert_lse_close(lse.cpu().numpy(), ol, what="fork")
+    # dropping B's references frees only B's private pages
+    free0 = pool.free_count()
+    assert pool.release(hA[:6] + [hB6, hB7]) == PA_OK and pool.free_count() == free0 + 2
+
+
+def test_shared_prefix_batch_sampled():
+    """Eight sequences sharing a 32K-row prompt's pages: sampled heads match
+    the oracle, and sharing leaves results equal to a private copy of the
+    prefix (the contiguous layout)."""
+    w = W.shared_prefix(n_seq=8, prefix=4096, own=300)
+    go, gl = run_decode(w)
+    pairs = [(0, 0), (1, 9), (4, 17), (7, 23)]
+    oo, ol = oracle.decode_workload(w, n_threads=THREADS, select=_sampled(w, pairs))
+    for s, h in pairs:
+        assert_close(go[s, :, h], oo[s, :, h], what=f"shared s{s} h{h}")
+        assert_lse_close(gl[s, :, h], ol[s, :, h], what=f"shared s{s} h{h}")
+    co, cl = run_decode(w.contiguous())
+    assert np.array_equal(go, co) and np.array_equal(gl, cl)

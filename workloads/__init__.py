@@ -310,6 +310,32 @@ def config(idx: int, n_qtok: int | None = None, variant: str = "") -> Workload:
     raise ValueError((idx, variant))
 
 
+def shared_prefix(n_seq: int = 8, prefix: int = 32768, own: int = 1024, ps: int = 16, k_type: int = TYPE_Q4_0,
+                  v_type: int = TYPE_Q4_0, n_qtok: int = 1, seed: int = 7) -> Workload:
+    """Prefix sharing (lucebox PR #555, roadmap item 6): n_seq sequences forked
+    from one prompt of `prefix` rows (a multiple of ps) whose pages they all
+    share, each followed by `own` rows of its own.  The prefix pages are
+    blocks 0 .. prefix/ps - 1; the own pages follow, interleaved across
+    sequences.  Logical rows are stored per sequence, so the prefix rows repeat
+    (identical bytes) in k_rows / v_rows."""
+    assert prefix % ps == 0
+    rng = np.random.default_rng(seed)
+    n_pre = prefix // ps
+    pre_k = random_rows(rng, prefix, k_type)
+    pre_v = random_rows(rng, prefix, v_type)
+    own_k = [random_rows(rng, own, k_type) for _ in range(n_seq)]
+    own_v = [random_rows(rng, own, v_type) for _ in range(n_seq)]
+    own_lists = interleaved_blocks([own] * n_seq, ps)
+    lists = [list(range(n_pre)) + [n_pre + b for b in own_lists[s]] for s in range(n_seq)]
+    lengths = np.full(n_seq, prefix + own, np.int32)
+    k_rows = np.concatenate([np.concatenate([pre_k, own_k[s]]) for s in range(n_seq)])
+    v_rows = np.concatenate([np.concatenate([pre_v, own_v[s]]) for s in range(n_seq)])
+    q = rng.standard_normal((n_seq, n_qtok, HQ, D), dtype=np.float32)
+    n_blocks = n_pre + sum(len(l) for l in own_lists)
+    return Workload(f"shared-prefix-{n_seq}x{prefix // 1024}k+{own}", lengths, n_qtok, ps, n_blocks, k_type, v_type,
+                    table_from_lists(lists), k_rows, v_rows, q, SCALE, {"seed": seed, "layout": "shared prefix"})
+
+
 PERCALL_LENGTHS = (32768, 131072, 262144)
 
 
