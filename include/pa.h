@@ -210,20 +210,22 @@ pa_status pa_append_rows_f16(const pa_pool* pool, void* k_pool, void* v_pool, co
 
 /* ------------------------------------------------------------------ decode
  * Single-step GQA decode attention over a paged cache: split-K flash decoding
- * through a block table, with a log-sum-exp merge of the splits ("Split-K
- * flash decoding for head size 256, GQA 6 and 1-4 query tokens (MTP verify
- * widths)", llama.cpp fork PR #2; "stable split-softmax merge", lucebox
- * PR #555, Summary).
+ * through a block table, with a log-sum-exp merge of the splits (llama.cpp
+ * fork PR #2, split-K decode commit: head size 256, GQA 6, one to four query
+ * tokens for speculative verification, and a later commit taking batches of
+ * up to eight tokens; lucebox PR #555, Summary: a numerically stable merge
+ * of split softmaxes).
  *
  * For sequence s with L = seq_lens[s] cached rows (the n_qtok new rows
  * included), query token t in [0, n_qtok) sits at position L - n_qtok + t and
  * attends to keys 0 .. L - n_qtok + t.  Query head h reads KV head
  * h / (n_q_heads / n_kv_heads).  Logits are scale * q.k; the output is the
  * softmax-weighted sum of V rows, and lse the natural-log log-sum-exp of the
- * scaled, masked logits ("max + log(rowsum)", llama.cpp fork PR #2, LSE
- * commit).  A row with no visible key would give out = 0 and lse = -inf.
+ * scaled, masked logits (llama.cpp fork PR #2, LSE commit: the row maximum
+ * plus the log of the row sum).  A row with no visible key would give
+ * out = 0 and lse = -inf.
  *
- * Supported: head_dim 256, n_q_heads / n_kv_heads = 6, n_qtok 1..4, K and V
+ * Supported: head_dim 256, n_q_heads / n_kv_heads = 6, n_qtok 1..8, K and V
  * each F16, Q4_0 or Q8_0 (PA_ERR_UNSUPPORTED otherwise).
  *
  * q:            device fp32 [n_seq][n_qtok][n_q_heads][head_dim], 16-byte aligned.

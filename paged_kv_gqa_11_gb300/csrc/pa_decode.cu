@@ -224,7 +224,7 @@ int type_slot(int t) { return t == PA_F16 ? 0 : t == PA_Q4_0 ? 1 : t == PA_Q8_0 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 int g_sms[kMaxDevices];
-int g_occ[kMaxDevices][3][3][3];  // [device][k][v][nt-1] CTAs per SM, 0 = not queried
+int g_occ[kMaxDevices][3][3][kMaxNT];  // [device][k][v][nt-1] CTAs per SM, 0 = not queried
 
 pa_status device_caps(int device, int kt, int vt, int nt, const KernelInfo& ki, int* sms, int* occ) {
   if (device < 0 || device >= kMaxDevices) return PA_ERR_INVALID;
@@ -256,7 +256,7 @@ pa_status check_shape(const pa_pool* pool, uint32_t n_qtok, uint32_t n_q_heads, 
   pa_pool_get_desc(pool, d);
   if (d->head_dim != kD) return PA_ERR_UNSUPPORTED;
   if (n_q_heads == 0 || n_q_heads != d->n_kv_heads * kGqa) return PA_ERR_UNSUPPORTED;
-  if (n_qtok < 1 || n_qtok > 4) return PA_ERR_UNSUPPORTED;
+  if (n_qtok < 1 || n_qtok > kMaxQTok) return PA_ERR_UNSUPPORTED;
   KernelInfo ki;
   if (!lookup_kernel(d->k_type, d->v_type, (kGqa * n_qtok + 7) / 8, &ki)) return PA_ERR_UNSUPPORTED;
   return PA_OK;
@@ -346,7 +346,7 @@ size_t workspace_bytes(long long max_ctas, long long n_seg, int R) { return work
 extern "C" size_t pa_decode_workspace_size(const pa_pool* pool, uint32_t n_seq, uint32_t n_qtok, int device) {
   pa_pool_desc d;
   if (pa_pool_get_desc(pool, &d) != PA_OK) return 0;
-  if (d.head_dim != kD || n_qtok < 1 || n_qtok > 4) return 0;
+  if (d.head_dim != kD || n_qtok < 1 || n_qtok > kMaxQTok) return 0;
   const int nt = (kGqa * (int)n_qtok + 7) / 8;
   KernelInfo ki;
   if (!lookup_kernel(d.k_type, d.v_type, nt, &ki)) return 0;
@@ -392,7 +392,7 @@ extern "C" pa_status pa_decode_plan(const pa_pool* pool, const int32_t* seq_lens
   pa_pool_desc d;
   if (!pool || (n_seq && !seq_lens_host)) return PA_ERR_INVALID;
   pa_pool_get_desc(pool, &d);
-  if (d.head_dim != kD || n_qtok < 1 || n_qtok > 4) return PA_ERR_UNSUPPORTED;
+  if (d.head_dim != kD || n_qtok < 1 || n_qtok > kMaxQTok) return PA_ERR_UNSUPPORTED;
   if (n_seq == 0) return PA_ERR_INVALID;
   KernelInfo ki;
   Plan plan{};

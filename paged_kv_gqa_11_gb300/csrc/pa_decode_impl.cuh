@@ -77,6 +77,8 @@ constexpr int kD = 256;       // head dim
 constexpr int kGqa = 6;       // query heads per KV head
 constexpr int kTile = 64;     // keys per per-head tile (two or more query tokens)
 constexpr int kTileHG = 16;   // keys per head-group tile (one query token)
+constexpr int kMaxQTok = 8;   // query tokens per sequence (speculative-verify widths)
+constexpr int kMaxNT = (kGqa * kMaxQTok + 7) / 8;  // n-tiles of 8 query rows: 6
 constexpr int kCWarps = 4;    // consumer warps = heads per head group (at most)
 constexpr int kThreads = (kCWarps + 1) * 32;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -116,7 +118,7 @@ constexpr int extras_bytes(int NT) {
 template <int KT, int VT, int NT>
 struct CtaTarget {
   static constexpr int kStageBytes = StageGeo<KT, VT>::kBytes;
-  static constexpr int kN = (kStageBytes <= 20000 && NT == 1) ? 3 : (kStageBytes <= 40000 ? 2 : 1);
+  static constexpr int kN = NT > 3 ? 1 : (kStageBytes <= 20000 && NT == 1) ? 3 : (kStageBytes <= 40000 ? 2 : 1);
 };
 
 template <int KT, int VT, int NT>

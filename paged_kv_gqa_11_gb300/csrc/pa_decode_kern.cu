@@ -1,8 +1,8 @@
 // Split-decode kernels for one (K format, V format) pair, chosen at compile
 // time with -DPA_KT=<pa_type> -DPA_VT=<pa_type>; the build compiles this file
 // once per pair, so the nine pairs compile in parallel.  Each unit defines
-// lookup_kernel_<K>_<V>, returning the kernel for 1, 2 or 3 n-tiles of query
-// rows (1 token, 2 tokens, 3-4 tokens).
+// lookup_kernel_<K>_<V>, returning the kernel for 1 to 6 n-tiles of 8 query
+// rows (6 rows per token: 1, 2, 3-4, 5, 6, 7-8 tokens).
 #include "pa_decode_impl.cuh"
 
 #if !defined(PA_KT) || !defined(PA_VT)
@@ -19,6 +19,9 @@ bool PA_LOOKUP_NAME(PA_KT, PA_VT)(int nt, KernelInfo* out) {
     case 1: *out = kernel_info<PA_KT, PA_VT, 1>(); return true;
     case 2: *out = kernel_info<PA_KT, PA_VT, 2>(); return true;
     case 3: *out = kernel_info<PA_KT, PA_VT, 3>(); return true;
+    case 4: *out = kernel_info<PA_KT, PA_VT, 4>(); return true;
+    case 5: *out = kernel_info<PA_KT, PA_VT, 5>(); return true;
+    case 6: *out = kernel_info<PA_KT, PA_VT, 6>(); return true;
     default: return false;
   }
 }

@@ -38,6 +38,10 @@ SMALL = [
     ("q4-mix-2tok", [2048, 333, 17, 4096], 64, Q4, Q4, 2, "shuffled"),
     ("q8-min-len", [1, 2, 3], 16, Q8, Q8, 1, "shuffled"),
     ("f16-min-len-4tok", [4, 5, 6, 67], 16, F16, F16, 4, "shuffled"),
+    ("q4-5tok", [300, 77, 5], 16, Q4, Q4, 5, "shuffled"),
+    ("f16-6tok", [200, 7, 6], 32, F16, F16, 6, "interleaved"),
+    ("q8-7tok", [130, 8, 65], 16, Q8, Q8, 7, "shuffled"),
+    ("q8k-q4v-8tok", [500, 9, 64], 256, Q8, Q4, 8, "shuffled"),
 ]
 
 
@@ -145,8 +149,10 @@ def test_page_size_invariance_and_repeats():
             assert np.array_equal(o, ref_o) and np.array_equal(l, ref_l), ps
 
 
-@pytest.mark.parametrize("nq", [1, 2, 3, 4])
+@pytest.mark.parametrize("nq", [1, 2, 3, 4, 5, 6, 7, 8])
 def test_config4_verify(nq):
+    """The verify workload at one to four tokens, and at five to eight (the
+    wider verify batches the fork's decode kernel later took)."""
     w = W.config(4, n_qtok=nq)
     go, gl = run_decode(w)
     sel = _sampled(w, [(s, h) for s in range(4) for h in (0, 5, 6, 17, 23)])
