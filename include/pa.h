@@ -85,9 +85,9 @@ typedef uint64_t pa_block;
 typedef struct pa_pool pa_pool;
 
 /* ------------------------------------------------------------------ allocator
- * "An exact fixed-block paged K/V allocator (transactional allocation,
- * stale-handle detection, immediate release)" -- lucebox PR #555, Summary.
- * Host metadata only; the K and V pools themselves are device buffers of
+ * lucebox PR #555, Summary: an exact allocator of fixed-size K/V blocks whose
+ * allocations are transactional, whose stale handles are detected and whose
+ * releases take effect at once.  Host metadata only; the K and V pools themselves are device buffers of
  * pa_pool_bytes() bytes that the caller allocates.  Thread-safe (one mutex
  * per pool). */
 

@@ -8,26 +8,27 @@
  * What it computes (each step cites the passage it follows):
  *
  *  - Row formats.  K and V rows are stored as ggml F16, Q4_0 or Q8_0 blocks
- *    ("a CUDA/HIP GGML_OP_PAGED_ATTN decode op for D=256 GQA with F16, Q4_0,
- *    and Q8_0 K/V", lucebox PR #555, Summary).  Q4_0: fp16 scale d then 16
+ *    (lucebox PR #555, Summary: the decode op covers head size 256 with GQA
+ *    and K/V in those three formats).  Q4_0: fp16 scale d then 16
  *    bytes, byte j holding element j (low nibble) and element j+16 (high
  *    nibble), value (nibble-8)*d; 18 bytes per 32 values, which is what the
  *    capacity table of lucebox PR #555 (K/V capacity: 207 MiB paged vs 1152
  *    MiB padded) implies.  Q8_0: fp16 d then 32 int8 q, value q*d.  The
  *    nibble order is a reading (ggml's layout); the pages do not print it.
  *
- *  - Gather through the page table.  "k/v are a pool of pages, and each
- *    logical page is either a pool page ..." (llama.cpp fork PR #2,
+ *  - Gather through the page table.  K and V live in a pool of pages and a
+ *    table maps each logical page to one of them (llama.cpp fork PR #2,
  *    ggml_flash_attn_ext_set_pages commit); every row address comes from the
  *    table, the page stride and the positions per page (TensorFold #1156,
  *    Design / Kernels, kv_row()).  Which bytes of the pool hold a row is this
  *    library's own choice (the pages print no byte layout); it is written out
  *    in orc_group_offset below.
  *
- *  - Attention.  Query head h uses KV head h / (Hq/Hkv) ("GQA 6", llama.cpp
- *    fork PR #2, split-K decode commit; contiguous grouping is a reading).
- *    Query token t of n_qtok sees keys 0..L-n_qtok+t (causal among the verify
- *    tokens, same commit: "1-4 query tokens (MTP verify widths)").  Logits
+ *  - Attention.  Query head h uses KV head h / (Hq/Hkv) (GQA with six query
+ *    heads per KV head, llama.cpp fork PR #2, split-K decode commit;
+ *    contiguous grouping is a reading).  Query token t of n_qtok sees keys
+ *    0..L-n_qtok+t (causal among the speculative-verify tokens of the same
+ *    commit, one to four of them, later up to eight).  Logits
  *    z_j = scale * q.k_j; two-pass softmax in float64: m = max z, w = exp(z-m),
  *    out = sum w v / sum w, and the log-sum-exp m + ln(sum w) in the natural-log
  *    units of the scaled, masked logits (llama.cpp fork PR #2, LSE commit).
@@ -37,8 +38,9 @@
  *  - Split merge (used by the self-tests only): partials over disjoint key
  *    ranges, each (m_i, l_i, o_i) with o_i normalised, combine by
  *    M = max m_i, w_i = l_i exp(m_i - M), out = sum w_i o_i / sum w_i,
- *    lse = M + ln(sum w_i)  (llama.cpp fork PR #2, LSE commit: "attend to parts
- *    of K/V separately and merge the normalized results exactly").
+ *    lse = M + ln(sum w_i)  (llama.cpp fork PR #2, LSE commit: partial
+ *    attentions over parts of K/V combine exactly once each carries its
+ *    log-sum-exp).
  *
  *  - Scatter (append): row (seq, pos) goes to block table[seq][pos/ps], slot
  *    pos%ps (colibri PR #372, Summary: upload new rows, scatter them into

@@ -1,7 +1,8 @@
 // Append: scatter newly written K/V rows into their page slots.
 //
-// colibri PR #372 (Summary): "upload only newly appended KV rows through one
-// packed transfer and scatter kernel".  The caller uploads the new rows once,
+// colibri PR #372 (Summary): only the rows a step appends cross to the
+// device, in one packed transfer, and a kernel scatters them.  The caller
+// uploads the new rows once,
 // packed as [n_rows][n_kv_heads][row_bytes] in their ggml format; this kernel
 // places each (row, head) in block table[seq][pos / page_size], slot
 // pos % page_size, arranging its bytes in the pool's row-group layout

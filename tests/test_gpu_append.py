@@ -1,6 +1,7 @@
 """Append/scatter kernel: byte-exact against the oracle's host scatter, and a
-resident multi-step append equals a one-shot upload (colibri PR #372:
-"a multi-step decode that stays token-identical to the non-resident path")."""
+resident multi-step append equals a one-shot upload (colibri PR #372: a
+resident cache advanced step by step must match the path that uploads
+everything)."""
 import numpy as np
 import pytest
 import torch

@@ -195,8 +195,9 @@ def test_fully_masked_split_is_finite():
 
 
 def test_controls_are_red():
-    """A swapped table over correctly placed pages, and a planted row, must
-    both fail the comparison (TensorFold #1156: both controls red)."""
+    """Two controls that must fail the comparison (TensorFold #1156,
+    Verification): a table whose pages are swapped while the data stays in
+    place, and a planted wrong row."""
     w = W.make_workload("ctl", 99, [700, 300], 16, Q4, Q4, 1, "shuffled")
     oo, _ = oracle.decode_workload(w)
     cache, tab = device_cache(w)

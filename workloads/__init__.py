@@ -6,9 +6,8 @@ sequence lengths.  It holds none of the decode arithmetic (no dequantisation,
 no gather, no softmax) so that both the float64 oracle and the CUDA library
 can consume the same inputs without sharing any of the method's code.
 
-Shapes follow the pages' Qwen attention dims: head size D=256, 24 query heads,
-4 KV heads (GQA 6) -- "All runs use Qwen attention dims (D=256, Hq=24, Hkv=4)"
-(lucebox PR #555, Benchmark results).
+Shapes follow the Qwen attention dims every benchmark of lucebox PR #555
+(Benchmark results) uses: head size D=256, 24 query heads, 4 KV heads (GQA 6).
 
 Quantiser (a reading: the pages name the formats but not a quantiser; any
 deterministic quantiser is valid because both sides consume the same bytes):
