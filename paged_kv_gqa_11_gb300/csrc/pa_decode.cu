@@ -32,46 +32,119 @@ namespace {
 // with l_i = 0 (every key masked) carry no weight; if all are empty the row is
 // 0 with lse -inf (the pd_combine fix in the same fork).
 //
-// Two levels in one launch, so a segment cut into hundreds of pieces (a long
-// sequence spread over the whole GPU) still merges with every SM pulling data.
-// A task is a chunk of up to 32 consecutive pieces of one multi-piece segment;
-// the host lists the tasks in the launch parameters and the grid holds one CTA
-// per (task, row).  Level 1: warp w loads its four pieces (partial and (m, l))
-// in one go and folds them against its own maximum; one barrier later 64
-// threads fold the eight warps, a float4 of dims each.  A segment with one
-// chunk writes its result directly; otherwise each chunk stores (M, W, O) at
-// its first piece's slot and the last chunk to arrive (a counter the split
-// kernel zeroed) folds the chunk results in chunk order, so the result does
-// not depend on timing.  Launched as a programmatic dependent of the split
-// kernel: the task decode runs before griddepcontrol.wait.
+// One level.  The host lists the multi-piece segments (task = segment, its
+// first CTA c0, its piece count np, how many ways its 256 dims are split, and
+// the task's first work item) in the launch parameters; the grid holds one
+// CTA per work item (task, row, dim split), found by a binary search over the
+// tasks' first items.  The CTA merges every piece of one row over
+// 256 / splits dims: its 256 threads form `cols` float4 columns x `groups`
+// piece groups (group q takes pieces q, q + groups, ...), so a long sequence
+// cut into hundreds of pieces is read with every load of a thread in flight at
+// once, and folded with two barriers: the row maximum, then the sums over the
+// groups.  The fold order is fixed, so the result does not depend on timing.
+// Launched as a programmatic dependent of the split kernel.
 constexpr int kMergeThreads = 256;
 constexpr int kMergeWarps = kMergeThreads / 32;
-constexpr int kChunk = 32;                      // pieces per task
-constexpr int kPerWarp = kChunk / kMergeWarps;  // pieces per warp
-constexpr int kMaxTasks = 1024;                 // bounded by about 1.04 x the split grid
+constexpr int kMaxSplits = 32;     // dims split up to 32 ways (8 dims, 2 float4 per CTA)
+constexpr int kMaxPerThread = 6;   // pieces a thread holds in one round
+constexpr int kMaxTasks = 1024;    // multi-piece segments: fewer than the split grid's CTAs
 
-// Task word: c0 (first CTA holding a piece of the segment) << 17 | chunk << 11 | pieces.
-struct MergeParams {
-  DecodeParams p;
-  int2 task[kMaxTasks];  // {segment, packed word}
+struct MergeTask {
+  int seg, c0, np, splits, first_item;
 };
 
-__device__ __forceinline__ float4 f4_fma(float f, float4 x, float4 acc) {
-  return make_float4(fmaf(f, x.x, acc.x), fmaf(f, x.y, acc.y), fmaf(f, x.z, acc.z), fmaf(f, x.w, acc.w));
+struct MergeParams {
+  DecodeParams p;
+  int n_tasks;
+  MergeTask task[kMaxTasks];
+};
+
+// Dim splits for a segment of np pieces: the fewest for which a thread holds
+// at most kMaxPerThread pieces (4 * splits piece groups).
+__host__ __device__ constexpr int merge_splits(int np) {
+  int sp = 1;
+  while (sp < kMaxSplits && np > 4 * sp * kMaxPerThread) sp *= 2;
+  return sp;
 }
 
 __global__ void __launch_bounds__(kMergeThreads) pa_merge_kernel(const __grid_constant__ MergeParams mp) {
   const DecodeParams& p = mp.p;
-  __shared__ float wm[kMergeWarps], ww[kMergeWarps];
-  __shared__ float4 part[kMergeWarps][kD / 4];
-  __shared__ int is_last;
+  __shared__ float red_m[kMergeWarps];
+  __shared__ float4 part[kMergeThreads];
+  __shared__ float red_w[kMergeThreads];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int row = blockIdx.y, R = p.rows_per_seg;
-  const int2 tk = mp.task[blockIdx.x];
-  const int seg = tk.x, c0 = tk.y >> 17, chunk = (tk.y >> 11) & 63, np = tk.y & 2047;
-  const int n_chunks = (np + kChunk - 1) / kChunk;
-  const int cbeg = c0 + kChunk * chunk, cend = min(c0 + np, cbeg + kChunk);  // pieces [cbeg, cend)
+  // task of this work item: the last whose first item is <= blockIdx.x
+  int lo = 0, hi = mp.n_tasks - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (mp.task[mid].first_item <= (int)blockIdx.x) lo = mid; else hi = mid - 1;
+  }
+  const MergeTask tk = mp.task[lo];
+  const int seg = tk.seg, c0 = tk.c0, np = tk.np, splits = tk.splits;
+  const int local = (int)blockIdx.x - tk.first_item;
+  const int row = local / splits, split = local % splits, R = p.rows_per_seg;
+  // Every CTA waits for the split grid before it reads a partial (and before
+  // it exits, so the merge grid completing implies the split grid completed).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int cols = (kD / 4) / splits;  // float4 columns of this CTA: 64, 16 or 8
+  const int groups = kMergeThreads / cols;
+  const int col = tid % cols, grp = tid / cols;
+  const int col4 = split * cols + col;  // float4 index within the 256 dims
   const int s = seg / p.segs_per_seq, g = seg % p.segs_per_seq;
+
+  float M = -INFINITY, W = 0.f;  // this thread's running state over its pieces
+  float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int base = 0; base < np; base += groups * kMaxPerThread) {
+    float2 ml[kMaxPerThread];
+    float4 x[kMaxPerThread];
+#pragma unroll
+    for (int i = 0; i < kMaxPerThread; ++i) {
+      const int c = base + grp + groups * i;
+      ml[i] = make_float2(-INFINITY, 0.f);
+      x[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (c < np) {
+        const long long slot = (long long)(c0 + c + seg) * R + row;
+        ml[i] = __ldcg(p.part_ml + slot);
+        x[i] = __ldcg(reinterpret_cast<const float4*>(p.part_o + slot * kD) + col4);
+      }
+    }
+    float mr = M;
+#pragma unroll
+    for (int i = 0; i < kMaxPerThread; ++i)
+      if (ml[i].y > 0.f) mr = fmaxf(mr, ml[i].x);
+    const float sa = (W > 0.f) ? exp2f(M - mr) : 0.f;  // earlier rounds, relative to the new maximum
+    W *= sa;
+    O = make_float4(O.x * sa, O.y * sa, O.z * sa, O.w * sa);
+#pragma unroll
+    for (int i = 0; i < kMaxPerThread; ++i) {
+      const float f = (ml[i].y > 0.f) ? exp2f(ml[i].x - mr) : 0.f;
+      W = fmaf(f, ml[i].y, W);
+      O = make_float4(fmaf(f, x[i].x, O.x), fmaf(f, x[i].y, O.y), fmaf(f, x[i].z, O.z), fmaf(f, x[i].w, O.w));
+    }
+    M = mr;
+  }
+  // ---- the row maximum over every piece
+  float mx = M;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if (lane == 0) red_m[warp] = mx;
+  __syncthreads();
+  float Mrow = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < kMergeWarps; ++i) Mrow = fmaxf(Mrow, red_m[i]);
+  const float f = (W > 0.f) ? exp2f(M - Mrow) : 0.f;
+  part[tid] = make_float4(O.x * f, O.y * f, O.z * f, O.w * f);
+  red_w[tid] = W * f;
+  __syncthreads();
+  // ---- sums over the piece groups, in group order (threads of column col)
+  if (tid >= cols) return;
+  float Wt = 0.f;
+  float4 Ot = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int q = 0; q < groups; ++q) {
+    const float4 v = part[q * cols + col];
+    Ot = make_float4(Ot.x + v.x, Ot.y + v.y, Ot.z + v.z, Ot.w + v.w);
+    Wt += red_w[q * cols + col];
+  }
   // Segment row -> output row: a head group's rows are (head, query head) of
   // one token; a single head's rows are (token, query head).
   long long orow;
@@ -81,130 +154,9 @@ __global__ void __launch_bounds__(kMergeThreads) pa_merge_kernel(const __grid_co
     const int t = row / kGqa, hl = row % kGqa;
     orow = ((long long)s * p.n_qtok + t) * p.n_q_heads + g * kGqa + hl;
   }
-  // Every CTA waits for the split grid before it reads a partial (and before
-  // it exits, so the merge grid completing implies the split grid completed).
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-
-  // ---- level 1: warp w folds pieces cbeg + 4w + k against its own maximum
-  float2 ml[kPerWarp];
-  float4 x0[kPerWarp], x1[kPerWarp];
-#pragma unroll
-  for (int k = 0; k < kPerWarp; ++k) {
-    const int c = cbeg + kPerWarp * warp + k;
-    ml[k] = make_float2(-INFINITY, 0.f);
-    x0[k] = x1[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (c < cend) {
-      const long long slot = (long long)(c + seg) * R + row;
-      ml[k] = __ldcg(p.part_ml + slot);
-      const float4* src = reinterpret_cast<const float4*>(p.part_o + slot * kD);
-      x0[k] = __ldcg(src + 2 * lane);
-      x1[k] = __ldcg(src + 2 * lane + 1);
-    }
-  }
-  float mw = -INFINITY;
-#pragma unroll
-  for (int k = 0; k < kPerWarp; ++k)
-    if (ml[k].y > 0.f) mw = fmaxf(mw, ml[k].x);
-  float wsum = 0.f;
-  float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
-#pragma unroll
-  for (int k = 0; k < kPerWarp; ++k) {
-    const float f = (ml[k].y > 0.f) ? exp2f(ml[k].x - mw) : 0.f;
-    wsum = fmaf(f, ml[k].y, wsum);
-    a0 = f4_fma(f, x0[k], a0);
-    a1 = f4_fma(f, x1[k], a1);
-  }
-  part[warp][2 * lane] = a0;
-  part[warp][2 * lane + 1] = a1;
-  if (lane == 0) { wm[warp] = mw; ww[warp] = wsum; }
-  __syncthreads();
-  // Fold the warps (64 threads, one float4 of dims each).
-  float M = -INFINITY, W = 0.f;
-  float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (tid < kD / 4) {
-#pragma unroll
-    for (int i = 0; i < kMergeWarps; ++i)
-      if (ww[i] > 0.f) M = fmaxf(M, wm[i]);
-#pragma unroll
-    for (int i = 0; i < kMergeWarps; ++i) {
-      const float f = (ww[i] > 0.f) ? exp2f(wm[i] - M) : 0.f;
-      W = fmaf(f, ww[i], W);
-      O = f4_fma(f, part[i][tid], O);
-    }
-  }
-
-  if (n_chunks > 1) {
-    const long long mslot = (long long)(cbeg + seg) * R + row;
-    if (tid < kD / 4) reinterpret_cast<float4*>(p.mid_o + mslot * kD)[tid] = O;
-    if (tid == 0) p.mid_ml[mslot] = make_float2(M, W);
-    __syncthreads();
-    if (tid == 0) {
-      __threadfence();  // cumulative: publishes the CTA's stores ordered before it by the barrier
-      is_last = atomicAdd(p.merge_count + (long long)seg * R + row, 1) == n_chunks - 1;
-    }
-    __syncthreads();
-    if (!is_last) return;
-    __threadfence();
-    // ---- level 2: the chunk results, in chunk order.  Quarter q (64 threads,
-    // a float4 of dims each) folds chunks q, q + 4, ... with every load in
-    // flight at once, then 64 threads fold the quarters.
-    const int q = tid >> 6, d4 = tid & 63;
-    constexpr int kPerQ = 4;  // chunks per quarter per round (16 per round)
-    float mq = -INFINITY, wq = 0.f;
-    float4 oq = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int base = 0; base < n_chunks; base += 4 * kPerQ) {
-      float2 cm[kPerQ];
-      float4 cy[kPerQ];
-#pragma unroll
-      for (int i = 0; i < kPerQ; ++i) {
-        const int k = base + q + 4 * i;
-        cm[i] = make_float2(-INFINITY, 0.f);
-        cy[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (k < n_chunks) {
-          const long long ms = (long long)(c0 + kChunk * k + seg) * R + row;
-          cm[i] = __ldcg(p.mid_ml + ms);
-          cy[i] = __ldcg(reinterpret_cast<const float4*>(p.mid_o + ms * kD) + d4);
-        }
-      }
-      float mr = mq;
-#pragma unroll
-      for (int i = 0; i < kPerQ; ++i)
-        if (cm[i].y > 0.f) mr = fmaxf(mr, cm[i].x);
-      const float sa = (wq > 0.f) ? exp2f(mq - mr) : 0.f;  // rescale the earlier rounds
-      wq *= sa;
-      oq = make_float4(oq.x * sa, oq.y * sa, oq.z * sa, oq.w * sa);
-#pragma unroll
-      for (int i = 0; i < kPerQ; ++i) {
-        const float f = (cm[i].y > 0.f) ? exp2f(cm[i].x - mr) : 0.f;
-        wq = fmaf(f, cm[i].y, wq);
-        oq = f4_fma(f, cy[i], oq);
-      }
-      mq = mr;
-    }
-    part[q][d4] = oq;
-    if (d4 == 0) { wm[q] = mq; ww[q] = wq; }
-    __syncthreads();
-    if (tid >= kD / 4) return;
-    M = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      if (ww[i] > 0.f) M = fmaxf(M, wm[i]);
-    W = 0.f;
-    O = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float f = (ww[i] > 0.f) ? exp2f(wm[i] - M) : 0.f;
-      W = fmaf(f, ww[i], W);
-      O = f4_fma(f, part[i][tid], O);
-    }
-    if (tid == 0) p.merge_count[(long long)seg * R + row] = 0;
-  } else if (tid >= kD / 4) {
-    return;
-  }
-
-  const float inv = W > 0.f ? 1.f / W : 0.f;
-  reinterpret_cast<float4*>(p.out + orow * kD)[tid] = make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
-  if (tid == 0 && p.lse) p.lse[orow] = W > 0.f ? (M + log2f(W)) * kLn2 : -INFINITY;
+  const float inv = Wt > 0.f ? 1.f / Wt : 0.f;
+  reinterpret_cast<float4*>(p.out + orow * kD)[col4] = make_float4(Ot.x * inv, Ot.y * inv, Ot.z * inv, Ot.w * inv);
+  if (split == 0 && col == 0 && p.lse) p.lse[orow] = Wt > 0.f ? (Mrow + log2f(Wt)) * kLn2 : -INFINITY;
 }
 
 // ------------------------------------------------------------------ host side
@@ -293,13 +245,16 @@ struct Plan {
   long long n_seg;
   long long slots;
   int merge_tasks;
+  long long merge_items;  // CTAs of the merge grid
 };
 
-// List the merge tasks (chunks of up to 32 pieces of every segment with more
-// than one piece) into task[]; returns their number, or -1 past kMaxTasks.
+// List the merge tasks (every segment with more than one piece) into task[];
+// returns their number, or -1 past kMaxTasks.  *n_items gets the number of
+// work items (CTAs of the merge grid).
 int list_merge_tasks(const int32_t* seq_lens_host, uint32_t n_seq, const Geometry& geo, long long tiles, int ctas,
-                     int2* task) {
+                     MergeTask* task, long long* n_items) {
   int n = 0;
+  long long items = 0;
   long long base = 0;
   for (uint32_t s = 0; s < n_seq; ++s) {
     const long long ntl = (seq_lens_host[s] + geo.tile_keys - 1) / geo.tile_keys;
@@ -308,34 +263,30 @@ int list_merge_tasks(const int32_t* seq_lens_host, uint32_t n_seq, const Geometr
       const int c0 = (int)(((a + 1) * ctas - 1) / tiles), c1 = (int)(((e + 1) * ctas - 1) / tiles);
       const int np = c1 - c0 + 1;
       if (np < 2) continue;
-      for (int k = 0; k * kChunk < np; ++k) {
-        if (n == kMaxTasks) return -1;
-        if (task) task[n] = make_int2((int)(s * geo.segs_per_seq + g), (c0 << 17) | (k << 11) | np);
-        ++n;
-      }
+      if (n == kMaxTasks) return -1;
+      const int sp = merge_splits(np);
+      if (task) task[n] = MergeTask{(int)(s * geo.segs_per_seq + g), c0, np, sp, (int)items};
+      items += (long long)sp * geo.rows_per_seg;
+      ++n;
     }
     base += ntl * geo.segs_per_seq;
   }
+  if (n_items) *n_items = items;
   return n;
 }
 
-// Workspace: piece partials (m, l) and O, the merge's level-1 results of the
-// same shape, and one arrival counter per (segment, row).
+// Workspace: the piece partials, (m, l) and O per (slot, row).
 struct WsLayout {
-  size_t ml, o, mid_ml, mid_o, count, total;
+  size_t ml, o, total;
 };
 
 WsLayout workspace_layout(long long max_ctas, long long n_seg, int R) {
   const long long slots = max_ctas + n_seg;
   auto up = [](size_t b) { return (b + 255) & ~size_t(255); };
   WsLayout w;
-  const size_t ml = up((size_t)slots * R * sizeof(float2)), o = up((size_t)slots * R * kD * sizeof(float));
   w.ml = 0;
-  w.o = ml;
-  w.mid_ml = ml + o;
-  w.mid_o = 2 * ml + o;
-  w.count = 2 * ml + 2 * o;
-  w.total = w.count + up((size_t)n_seg * R * sizeof(int));
+  w.o = up((size_t)slots * R * sizeof(float2));
+  w.total = w.o + up((size_t)slots * R * kD * sizeof(float));
   return w;
 }
 
@@ -377,12 +328,10 @@ static pa_status make_plan(const pa_pool_desc& d, const int32_t* seq_lens_host, 
   plan->ctas = (int)std::min<long long>(tiles, (long long)sms * occ);
   plan->n_seg = (long long)n_seq * geo.segs_per_seq;
   plan->slots = (long long)plan->ctas + plan->n_seg;
-  // The task word packs c0 < 2^14, chunk < 2^6 and np < 2^11; the task count
-  // is at most about 1.04 x the CTA count (each multi-piece segment holds a
-  // CTA boundary), below kMaxTasks for any grid of fewer than 2000 CTAs.
-  if (plan->ctas >= 2000) return PA_ERR_UNSUPPORTED;
-  plan->merge_tasks = list_merge_tasks(seq_lens_host, n_seq, geo, tiles, plan->ctas, nullptr);
-  if (plan->merge_tasks < 0) return PA_ERR_UNSUPPORTED;
+  // Each multi-piece segment holds a CTA boundary, so there are fewer merge
+  // tasks than CTAs: kMaxTasks covers any grid of up to 1024 CTAs.
+  plan->merge_tasks = list_merge_tasks(seq_lens_host, n_seq, geo, tiles, plan->ctas, nullptr, &plan->merge_items);
+  if (plan->merge_tasks < 0 || plan->merge_items >= (1ll << 31)) return PA_ERR_UNSUPPORTED;
   return PA_OK;
 }
 
@@ -462,10 +411,6 @@ static pa_status prepare_decode(const pa_pool* pool, const float* q, const void*
   const WsLayout lay = workspace_layout((long long)sms * occ, plan->n_seg, plan->geo.rows_per_seg);
   p.part_ml = reinterpret_cast<float2*>(ws + lay.ml);
   p.part_o = reinterpret_cast<float*>(ws + lay.o);
-  p.mid_ml = reinterpret_cast<float2*>(ws + lay.mid_ml);
-  p.mid_o = reinterpret_cast<float*>(ws + lay.mid_o);
-  p.merge_count = reinterpret_cast<int*>(ws + lay.count);
-  p.n_counters = (int)(plan->n_seg * plan->geo.rows_per_seg);
   p.total_tiles = plan->tiles;
   p.n_ctas = plan->ctas;
   p.n_seq = (int)n_seq;
@@ -508,11 +453,11 @@ static pa_status run_decode(int passes, PA_DECODE_ARGS) {
     if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
   }
   if ((passes & 2) && plan.merge_tasks > 0) {
-    static thread_local MergeParams mp;  // 8 KB: kept off the stack
+    static thread_local MergeParams mp;  // 20 KB: kept off the stack
     mp.p = p;
-    list_merge_tasks(seq_lens_host, n_seq, plan.geo, plan.tiles, plan.ctas, mp.task);
+    mp.n_tasks = list_merge_tasks(seq_lens_host, n_seq, plan.geo, plan.tiles, plan.ctas, mp.task, nullptr);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)plan.merge_tasks, (unsigned)plan.geo.rows_per_seg);
+    cfg.gridDim = dim3((unsigned)plan.merge_items);
     cfg.blockDim = dim3(kMergeThreads);
     cfg.stream = cs;
     cudaLaunchAttribute attr[1];
@@ -545,9 +490,8 @@ extern "C" pa_status pa_decode_merge(PA_DECODE_ARGS) { return run_decode(2, PA_D
 // That lookup runs once per device, with the device current, on the first
 // call there; the first call on a device should therefore come before any
 // stream capture.  Every call shares the array and it keeps the last call's
-// contents; the split kernel zeroes the merge counters itself, and partials
-// are written before they are read, so nothing has to be cleared between
-// calls.  Each GPU has its own copy of the array; calls whose work overlaps on
+// contents; partials are written before they are read, so nothing has to be
+// cleared between calls.  Each GPU has its own copy of the array; calls whose work overlaps on
 // one GPU (for example on two streams) race on it and must be serialised.
 static __device__ __align__(256) uint8_t pa_noalloc_scratch[PA_NOALLOC_SCRATCH_BYTES];
 

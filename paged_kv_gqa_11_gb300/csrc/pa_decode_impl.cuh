@@ -218,10 +218,6 @@ struct DecodeParams {
   int32_t* err;
   float2* part_ml;  // [slots][rows_per_seg] (m in log2 units, l)
   float* part_o;    // [slots][rows_per_seg][kD]
-  float2* mid_ml;   // [slots][rows_per_seg] merge level-1 results, indexed by a chunk's first slot
-  float* mid_o;     // [slots][rows_per_seg][kD]
-  int* merge_count; // [n_seg][rows_per_seg] level-1 arrivals; zeroed by the split kernel
-  int n_counters;   // n_seg * rows_per_seg
   long long total_tiles;
   int n_ctas;
   int n_seq;
@@ -1311,9 +1307,6 @@ __global__ void __launch_bounds__(kThreads, CtaTarget<KT, VT, NT>::kN)
   const int Gn = p.n_ctas;
   const long long a = (long long)blockIdx.x * T / Gn, b = (long long)(blockIdx.x + 1) * T / Gn;
 
-  // Zero the merge kernel's arrival counters (it reads them only after the
-  // whole split grid has finished).
-  for (int i = blockIdx.x * kThreads + tid; i < p.n_counters; i += gridDim.x * kThreads) p.merge_count[i] = 0;
   if (tid == 0) {
     // The merge kernel may launch now; it reads nothing of ours before its
     // griddepcontrol.wait.
