@@ -41,7 +41,8 @@ namespace {
 // piece groups (group q takes pieces q, q + groups, ...), so a long sequence
 // cut into hundreds of pieces is read with every load of a thread in flight at
 // once, and folded with two barriers: the row maximum, then the sums over the
-// groups.  The fold order is fixed, so the result does not depend on timing.
+// groups (within each warp by shuffles, then over the warps).  The fold order
+// is fixed, so the result does not depend on timing.
 // Launched as a programmatic dependent of the split kernel.
 constexpr int kMergeThreads = 256;
 constexpr int kMergeWarps = kMergeThreads / 32;
@@ -133,17 +134,33 @@ __global__ void __launch_bounds__(kMergeThreads) pa_merge_kernel(const __grid_co
 #pragma unroll
   for (int i = 0; i < kMergeWarps; ++i) Mrow = fmaxf(Mrow, red_m[i]);
   const float f = (W > 0.f) ? exp2f(M - Mrow) : 0.f;
-  part[tid] = make_float4(O.x * f, O.y * f, O.z * f, O.w * f);
-  red_w[tid] = W * f;
+  float Wt = W * f;
+  float4 Ot = make_float4(O.x * f, O.y * f, O.z * f, O.w * f);
+  // ---- sums over the piece groups, in a fixed order: first the groups
+  // within a warp (xor partners over the lane bits above the column bits),
+  // then the warps' sums in warp order.
+  const int wcols = cols < 32 ? cols : 32;  // columns a warp covers
+  for (int off = wcols; off < 32; off <<= 1) {
+    Wt += __shfl_xor_sync(0xffffffffu, Wt, off);
+    Ot.x += __shfl_xor_sync(0xffffffffu, Ot.x, off);
+    Ot.y += __shfl_xor_sync(0xffffffffu, Ot.y, off);
+    Ot.z += __shfl_xor_sync(0xffffffffu, Ot.z, off);
+    Ot.w += __shfl_xor_sync(0xffffffffu, Ot.w, off);
+  }
+  if (lane < wcols) {
+    part[warp * wcols + lane] = Ot;
+    red_w[warp * wcols + lane] = Wt;
+  }
   __syncthreads();
-  // ---- sums over the piece groups, in group order (threads of column col)
   if (tid >= cols) return;
-  float Wt = 0.f;
-  float4 Ot = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int q = 0; q < groups; ++q) {
-    const float4 v = part[q * cols + col];
+  // Warps holding column col: with cols >= 32, every (cols / 32)-th warp.
+  const int wstep = cols > 32 ? cols / 32 : 1, w0 = cols > 32 ? col / 32 : 0;
+  Wt = 0.f;
+  Ot = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int w = w0; w < kMergeWarps; w += wstep) {
+    const float4 v = part[w * wcols + col % wcols];
     Ot = make_float4(Ot.x + v.x, Ot.y + v.y, Ot.z + v.z, Ot.w + v.w);
-    Wt += red_w[q * cols + col];
+    Wt += red_w[w * wcols + col % wcols];
   }
   // Segment row -> output row: a head group's rows are (head, query head) of
   // one token; a single head's rows are (token, query head).
