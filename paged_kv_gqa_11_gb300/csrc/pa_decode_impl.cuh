@@ -37,13 +37,14 @@
 // raised only when a logit exceeds it by more than 2^8 (P <= 256 stays exact
 // enough in fp16), so most tiles rescale nothing.
 //
-// Two to four query tokens ("per-head" tiles, 12-24 rows).  Holding O for all
+// Two to eight query tokens ("per-head" tiles, 12-48 rows).  Holding O for all
 // dims per warp would take 64 registers per 8 rows, so the warps split the
 // tile instead: a segment is (sequence, KV head), a tile 64 keys (four row
-// groups) of that head; in the S phase warp w computes the keys of group w,
-// publishes its tile max, row sums and P (transposed with movmatrix) in shared
-// memory, and after a named barrier computes O^T for dims 64w..64w+63 over all
-// 64 keys.
+// groups) of that head; in the S phase warp w computes the keys of group w
+// against a reference maximum per row that the four warps share (raised, in
+// a rare second step, only when a logit passes it by 2^8), publishes P
+// (transposed with movmatrix) in shared memory, and after a named barrier
+// computes O^T for dims 64w..64w+63 over all 64 keys.
 //
 // Dequantisation.  K goes into the MMA as raw magic-biased halves: a Q4_0
 // nibble n becomes 1024+n (low) or 1024+16n (high nibble, against Q/16), a
@@ -260,10 +261,6 @@ struct Smem {
   static constexpr int kTotal = kMisc + 32;
   static constexpr int kLaunch = kTotal + kAlign;  // dynamic bytes requested (base aligned inside)
 };
-
-__device__ __forceinline__ int cta_of_tile(long long x, long long T, int G) {
-  return (int)(((x + 1) * (long long)G - 1) / T);
-}
 
 __device__ __forceinline__ int tiles_of(const DecodeParams& p, int L) { return (L + p.tile_keys - 1) / p.tile_keys; }
 
