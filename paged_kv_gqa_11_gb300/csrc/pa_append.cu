@@ -152,6 +152,9 @@ __device__ __forceinline__ void place_block_f16(int type, bool role_v, const uin
 // is a 32-value block, quantised to the pool's format.
 template <bool kF16In>
 __global__ void __launch_bounds__(256) pa_append_kernel(const __grid_constant__ AppendParams p) {
+  // A decode launched next may start its set-up now: it reads nothing before
+  // its griddepcontrol.wait, which waits for this grid to complete.
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;");
   const long long k_total = p.n_rows * p.n_kv_heads * p.k_units;
   const long long v_total = p.n_rows * p.n_kv_heads * p.v_units;
   const long long stride = (long long)gridDim.x * blockDim.x;

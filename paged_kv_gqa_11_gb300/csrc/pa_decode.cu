@@ -466,8 +466,20 @@ static pa_status run_decode(int passes, PA_DECODE_ARGS) {
   if (st != PA_OK) return st;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   if (passes & 1) {
-    ki.fn<<<plan.ctas, kThreads, ki.smem, cs>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+    // A programmatic dependent of the previous kernel on the stream: its
+    // launch and set-up overlap that kernel's tail (the split kernel waits for
+    // it before reading any input).
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)plan.ctas);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = (size_t)ki.smem;
+    cfg.stream = cs;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, ki.fn, p) != cudaSuccess) return PA_ERR_CUDA;
   }
   if ((passes & 2) && plan.merge_tasks > 0) {
     static thread_local MergeParams mp;  // 20 KB: kept off the stack

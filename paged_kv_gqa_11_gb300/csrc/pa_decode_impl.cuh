@@ -1303,6 +1303,10 @@ __global__ void __launch_bounds__(kThreads, CtaTarget<KT, VT, NT>::kN)
   const long long T = p.total_tiles;
   const int Gn = p.n_ctas;
   const long long a = (long long)blockIdx.x * T / Gn, b = (long long)(blockIdx.x + 1) * T / Gn;
+  // Launched as a programmatic dependent of the previous kernel on the stream
+  // (for example the append of this step's rows): every thread waits for it
+  // to complete before it reads any input.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   if (tid == 0) {
     // The merge kernel may launch now; it reads nothing of ours before its
