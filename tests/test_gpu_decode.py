@@ -330,3 +330,42 @@ def test_shared_prefix_batch_sampled():
         assert_lse_close(gl[s, :, h], ol[s, :, h], what=f"shared s{s} h{h}")
     co, cl = run_decode(w.contiguous())
     assert np.array_equal(go, co) and np.array_equal(gl, cl)
+
+
+def test_append_then_decode_back_to_back():
+    """Decode steps as a server runs them: each step appends one new row per
+    sequence and decodes at once on the same stream, with no host
+    synchronisation in between.  The decode is launched as a programmatic
+    dependent of the append and must still see every appended row: each
+    step's output matches the oracle on the rows present at that step."""
+    import dataclasses
+    steps = 6
+    lens_final = np.array([160, 97, 33], np.int32)
+    w = W.make_workload("back-to-back", 909, lens_final, 16, Q4, Q4, 1, "shuffled")
+    base = lens_final - steps
+
+    def rows(sel):
+        return (to_dev(w.k_rows[sel]), to_dev(w.v_rows[sel]), to_dev(w.row_seq[sel]), to_dev(w.row_pos[sel]))
+
+    cache = PagedKVCache(w.n_blocks, w.page_size, w.k_type, w.v_type)
+    tab = to_dev(w.table)
+    pos_limit = base[w.row_seq]
+    cache.append(*rows(w.row_pos < pos_limit), tab)
+    step_rows = [rows(w.row_pos == pos_limit + t) for t in range(steps)]  # uploaded before the loop
+    q = to_dev(w.q)
+    lens_dev = [to_dev(base + t + 1) for t in range(steps)]
+    torch.cuda.synchronize()
+    results = []
+    for t in range(steps):
+        cache.append(*step_rows[t], tab)
+        lens = base + t + 1
+        out, lse = cache.decode(q, tab, lens_dev[t], lens, 1, w.scale)
+        results.append((lens, out, lse))
+    torch.cuda.synchronize()
+    assert cache.check() == PA_OK
+    for lens, out, lse in results:
+        keep = w.row_pos < lens[w.row_seq]
+        wt = dataclasses.replace(w, seq_lens=lens.astype(np.int32), k_rows=w.k_rows[keep], v_rows=w.v_rows[keep])
+        oo, ol = oracle.decode_workload(wt)
+        assert_close(out.cpu().numpy(), oo, what=f"lengths {lens.tolist()}")
+        assert_lse_close(lse.cpu().numpy(), ol, what=f"lengths {lens.tolist()}")
