@@ -59,7 +59,7 @@ typedef struct CUstream_st* pa_stream_t;
 typedef enum {
   PA_OK = 0,
   PA_ERR_INVALID = 1,     /* bad argument: null pointer, size, alignment, length */
-  PA_ERR_UNSUPPORTED = 2, /* shape or format this build does not implement */
+  PA_ERR_UNSUPPORTED = 2, /* shape or format this library does not implement */
   PA_ERR_OOM = 3,         /* not enough free blocks; nothing was allocated */
   PA_ERR_STALE = 4,       /* a handle is released, unknown or repeated; nothing was released */
   PA_ERR_BOUNDS = 5,      /* device: a table entry or position outside the pool or table */
