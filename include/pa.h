@@ -247,7 +247,12 @@ pa_status pa_append_rows_f16(const pa_pool* pool, void* k_pool, void* v_pool, co
  *               read as zeros (no out-of-range read).
  * The result depends only on the inputs and on seq_lens (not on page size or
  * page placement): a paged cache and an identity-table cache holding the same
- * rows give bit-identical outputs. */
+ * rows give bit-identical outputs.
+ *
+ * Launches: the split kernel, then (when a sequence is split) the merge
+ * kernel, on `stream`.  Both are programmatic dependent launches: each may
+ * start while the previous kernel on the stream finishes, but waits for it to
+ * complete before reading anything, so stream order is kept. */
 pa_status pa_decode(const pa_pool* pool, const float* q, const void* k_pool, const void* v_pool,
                     const int32_t* block_table, uint32_t table_stride, const int32_t* seq_lens_dev,
                     const int32_t* seq_lens_host, uint32_t n_seq, uint32_t n_qtok,
@@ -273,8 +278,9 @@ pa_status pa_decode_merge(const pa_pool* pool, const float* q, const void* k_poo
                           pa_stream_t stream);
 
 /* Scratch bytes pa_decode needs for up to n_seq sequences of n_qtok query
- * tokens on CUDA device `device`, whatever their lengths ("report the scratch
- * up front so a tight budget fails at load", llama.cpp fork PR #2, scratch
+ * tokens on CUDA device `device`, whatever their lengths.  Reported up front
+ * so that a caller with a fixed memory budget can reserve it before the first
+ * step instead of failing in the middle of one (llama.cpp fork PR #2, scratch
  * commit).  0 for an unsupported shape. */
 size_t pa_decode_workspace_size(const pa_pool* pool, uint32_t n_seq, uint32_t n_qtok, int device);
 
