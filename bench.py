@@ -1,8 +1,8 @@
 #!/usr/bin/env python
 """Benchmark of paged GQA decode attention on GB300.
 
-Workload (default): the ragged 8-request decode of lucebox PR #555 ("Ragged
-8-request workload (128K + 7 x 8K, Q4_0 K/V)"): sequence lengths 131072 and
+Workload (default): the ragged eight-request decode of lucebox PR #555
+(Benchmark results, its ragged-workload table): sequence lengths 131072 and
 7 x 8192 (188,416 live tokens), 16-token pages handed out round-robin as if the
 requests arrived together, Q4_0 K/V from N(0,1) sources, D=256, 24 query heads
 on 4 KV heads, one query token.  Synthetic, seeded inputs.
