@@ -369,3 +369,39 @@ def test_append_then_decode_back_to_back():
         oo, ol = oracle.decode_workload(wt)
         assert_close(out.cpu().numpy(), oo, what=f"lengths {lens.tolist()}")
         assert_lse_close(lse.cpu().numpy(), ol, what=f"lengths {lens.tolist()}")
+
+
+def test_split_then_merge_equals_decode():
+    """pa_decode_split then pa_decode_merge on one stream is exactly
+    pa_decode (same arguments and workspace, nothing in between)."""
+    w = W.make_workload("split-merge", 77, [3000, 700, 41, 5000], 16, Q8, Q4, 3, "shuffled")
+    cache, tab = device_cache(w)
+    q = to_dev(w.q)
+    sl = to_dev(w.seq_lens)
+    o1, l1 = cache.decode(q, tab, sl, w.seq_lens, w.n_qtok, w.scale)
+    o2 = torch.full_like(o1, float("nan"))
+    l2 = torch.full_like(l1, float("nan"))
+    cache.decode(q, tab, sl, w.seq_lens, w.n_qtok, w.scale, out=o2, lse=l2, passes="split")
+    cache.decode(q, tab, sl, w.seq_lens, w.n_qtok, w.scale, out=o2, lse=l2, passes="merge")
+    torch.cuda.synchronize()
+    assert cache.check() == PA_OK
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_decode_reads_inputs_written_just_before():
+    """Q and the lengths are produced by kernels launched on the stream right
+    before the decode, with no synchronisation: the decode (a programmatic
+    dependent launch) still reads the values they write."""
+    w = W.make_workload("fresh-inputs", 78, [900, 64, 2000], 16, Q4, Q4, 1, "shuffled")
+    cache, tab = device_cache(w)
+    q_half = to_dev(w.q * 0.5)
+    sl_src = to_dev(w.seq_lens - 1)
+    torch.cuda.synchronize()
+    q = q_half * 2.0          # a kernel writing q
+    sl = sl_src + 1           # a kernel writing the device lengths
+    out, lse = cache.decode(q, tab, sl, w.seq_lens, w.n_qtok, w.scale)
+    torch.cuda.synchronize()
+    assert cache.check() == PA_OK
+    oo, ol = oracle.decode_workload(w)
+    assert_close(out.cpu().numpy(), oo, what="fresh inputs")
+    assert_lse_close(lse.cpu().numpy(), ol, what="fresh inputs")
