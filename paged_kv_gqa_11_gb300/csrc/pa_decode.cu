@@ -210,7 +210,7 @@ pa_status device_caps(int device, int kt, int vt, int nt, const KernelInfo& ki, 
     if (cur != device) cudaSetDevice(device);
     cudaError_t e = cudaFuncSetAttribute(ki.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, ki.smem);
     int n = 0;
-    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, ki.fn, kThreads, ki.smem);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, ki.fn, ki.threads, ki.smem);
     if (cur != device) cudaSetDevice(cur);
     if (e != cudaSuccess || n <= 0) return PA_ERR_CUDA;
     o = n;
@@ -471,7 +471,7 @@ static pa_status run_decode(int passes, PA_DECODE_ARGS) {
     // it before reading any input).
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)plan.ctas);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3((unsigned)ki.threads);
     cfg.dynamicSmemBytes = (size_t)ki.smem;
     cfg.stream = cs;
     cudaLaunchAttribute attr[1];

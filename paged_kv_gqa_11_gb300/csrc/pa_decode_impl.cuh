@@ -80,8 +80,12 @@ constexpr int kTile = 64;     // keys per per-head tile (two or more query token
 constexpr int kTileHG = 16;   // keys per head-group tile (one query token)
 constexpr int kMaxQTok = 8;   // query tokens per sequence (speculative-verify widths)
 constexpr int kMaxNT = (kGqa * kMaxQTok + 7) / 8;  // n-tiles of 8 query rows: 6
-constexpr int kCWarps = 4;    // consumer warps = heads per head group (at most)
-constexpr int kThreads = (kCWarps + 1) * 32;
+constexpr int kCWarps = 4;    // consumer warps per group (one-token path: = heads per head group, at most)
+// Threads of a split-kernel CTA: kG groups of consumer warps and one producer
+// warp.  Five to eight query tokens run two groups, each taking half of the
+// tokens, over one shared stage ring.
+__host__ __device__ constexpr int threads_of(int kG) { return (kCWarps * kG + 1) * 32; }
+constexpr int kThreads = threads_of(1);
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLazy = 8.0f;  // log2 headroom before the running max is raised
@@ -104,31 +108,32 @@ struct StageGeo {
   static_assert(kVGroup % Fmt<VT>::kRowQ == 0 && Fmt<VT>::kScales % Fmt<VT>::kRowQ == 0, "V group alignment");
 };
 
-// Shared memory outside the stage ring.
-constexpr int extras_bytes(int NT) {
-  return (NT == 1 ? kCWarps * (16 * 32 * 8 + 8 * 4 * 16)  // per-warp Q fragments + block corrections
-                  : (2 * 16 * NT * 32 * 8                  // Q fragments, double buffered
-                     + 2 * 8 * NT * 4 * 16                 // block corrections
-                     + 2 * kCWarps * NT * 32 * 8           // P fragments
-                     + 2 * kCWarps * NT * 8 * 8))          // tile stats
+// Shared memory outside the stage ring (kG consumer groups).
+constexpr int extras_bytes(int NT, int kG = 1) {
+  return (NT == 1 ? kCWarps * (16 * 32 * 8 + 8 * 4 * 16)        // per-warp Q fragments + block corrections
+                  : kG * (2 * 16 * NT * 32 * 8                   // Q fragments, double buffered
+                          + 2 * 8 * NT * 4 * 16                  // block corrections
+                          + 2 * kCWarps * NT * 32 * 8            // P fragments
+                          + 2 * kCWarps * NT * 8 * 8))           // tile stats
          + 2 * 8 * 8 + 32;  // barriers (up to 8 stages), misc
 }
 
 // CTAs per SM a configuration aims for: three for small one-token stages,
 // otherwise two, or one when a stage is large.
-template <int KT, int VT, int NT>
+template <int KT, int VT, int NT, int kG = 1>
 struct CtaTarget {
   static constexpr int kStageBytes = StageGeo<KT, VT>::kBytes;
-  static constexpr int kN = NT > 3 ? 1 : (kStageBytes <= 20000 && NT == 1) ? 3 : (kStageBytes <= 40000 ? 2 : 1);
+  static constexpr int kN = (NT > 3 || kG > 1) ? 1
+                            : (kStageBytes <= 20000 && NT == 1) ? 3 : (kStageBytes <= 40000 ? 2 : 1);
 };
 
-template <int KT, int VT, int NT>
+template <int KT, int VT, int NT, int kG = 1>
 struct Stages {
   static constexpr int kStageBytes = StageGeo<KT, VT>::kBytes;
-  static constexpr int kCtas = CtaTarget<KT, VT, NT>::kN;
+  static constexpr int kCtas = CtaTarget<KT, VT, NT, kG>::kN;
   static constexpr int kBudget = (233472 - kCtas * 1024) / kCtas;  // 228 KB per SM, 1 KB reserved per CTA
   static constexpr int kPerCtaMax = kBudget < 232448 ? kBudget : 232448;
-  static constexpr int kFit = (kPerCtaMax - extras_bytes(NT) - kAlign) / kStageBytes;
+  static constexpr int kFit = (kPerCtaMax - extras_bytes(NT, kG) - kAlign) / kStageBytes;
   static constexpr int kN = kFit > 8 ? 8 : kFit;
   static_assert(kN >= 2, "stage ring does not fit");
 };
@@ -236,9 +241,9 @@ struct DecodeParams {
 };
 
 // Shared-memory layout (byte offsets from the kAlign-aligned base).
-template <int KT, int VT, int NT>
+template <int KT, int VT, int NT, int kG = 1>
 struct Smem {
-  static constexpr int kStages = Stages<KT, VT, NT>::kN;
+  static constexpr int kStages = Stages<KT, VT, NT, kG>::kN;
   static constexpr int kKBytes = StageGeo<KT, VT>::kKBytes;
   static constexpr int kStageBytes = StageGeo<KT, VT>::kBytes;
   static constexpr int kRing = kStages * kStageBytes;
@@ -247,15 +252,17 @@ struct Smem {
   static constexpr int kWQBytes = 16 * 32 * 8;
   static constexpr int kWCb = kWQ + kCWarps * kWQBytes;
   static constexpr int kWCbBytes = 8 * 4 * 16;
-  // per-head path: Q fragments [2][16][NT][32] uint2, corrections [2][8][NT][4]
-  // float4, P fragments [2][4][NT][32] uint2, stats [2][4][NT*8] float2
+  // per-head path, per consumer group (group g at + g * kGrpBytes): Q fragments
+  // [2][16][NT][32] uint2, corrections [2][8][NT][4] float4, P fragments
+  // [2][4][NT][32] uint2, stats [2][4][NT*8] float2
   static constexpr int kQBuf = 16 * NT * 32 * 8;
   static constexpr int kQ = kRing;
   static constexpr int kCbBuf = 8 * NT * 4 * 16;
   static constexpr int kCb = kQ + 2 * kQBuf;
   static constexpr int kP = kCb + 2 * kCbBuf;
   static constexpr int kStat = kP + 2 * kCWarps * NT * 32 * 8;
-  static constexpr int kWorkEnd = NT == 1 ? kWCb + kCWarps * kWCbBytes : kStat + 2 * kCWarps * NT * 8 * 8;
+  static constexpr int kGrpBytes = kStat + 2 * kCWarps * NT * 8 * 8 - kQ;
+  static constexpr int kWorkEnd = NT == 1 ? kWCb + kCWarps * kWCbBytes : kQ + kG * kGrpBytes;
   static constexpr int kBar = kWorkEnd;                 // full[kStages], empty[kStages]
   static constexpr int kMisc = kBar + 2 * kStages * 8;  // abort flag, start position
   static constexpr int kTotal = kMisc + 32;
@@ -435,11 +442,11 @@ __device__ void produce_hg(const DecodeParams& p, uint32_t ring, uint32_t bar_fu
 // page; otherwise each group is its own run.  Groups past the last key are
 // not copied (the consumers mask those keys); a group whose table entry is
 // outside the pool is zero-filled and reported.
-template <int KT, int VT, int NT>
+template <int KT, int VT, int NT, int kG>
 __device__ void produce_head(const DecodeParams& p, uint32_t ring, uint32_t bar_full, uint32_t bar_empty,
                              volatile int* abort, long long a, long long b, TilePos pos) {
   using G = StageGeo<KT, VT>;
-  constexpr int kStages = Stages<KT, VT, NT>::kN;
+  constexpr int kStages = Stages<KT, VT, NT, kG>::kN;
   constexpr int RK = Fmt<KT>::kRow, RV = Fmt<VT>::kRow;
   const int lane = threadIdx.x & 31;
   const int ps = p.page_size, H = p.n_kv_heads;
@@ -575,13 +582,13 @@ __device__ __forceinline__ const float* q_row(const DecodeParams& p, int s, int 
 
 // Per-head path: stage Q of (sequence s, KV head g) as S-MMA B fragments in
 // the K format's dim order (high-nibble Q4_0 k-steps hold Q/16) and, for
-// quantised K, the block biases ([block][nt][t] float4).  All consumer
-// threads take part: the R query rows (1 KB each) are read as float4, all of
-// a thread's loads in flight at once; rows R .. 8*NT-1 of the fragments and
-// biases are zero.
+// quantised K, the block biases ([block][nt][t] float4).  The 128 threads of
+// one consumer group (tid 0..127) take part: the R query rows from segment row
+// row0 on (1 KB each) are read as float4, all of a thread's loads in flight at
+// once; rows R .. 8*NT-1 of the fragments and biases are zero.
 template <int KT, int NT>
-__device__ __noinline__ void stage_q(const DecodeParams& p, int s, int g, uint32_t qf, float* cb4, int tid) {
-  const int R = kGqa * p.n_qtok;
+__device__ __noinline__ void stage_q(const DecodeParams& p, int s, int g, uint32_t qf, float* cb4, int tid, int row0,
+                                     int R) {
   constexpr int kN = kCWarps * 32;
   constexpr int kLoads = (NT * 8 * kD / 4 + kN - 1) / kN;  // float4 per thread covering 8*NT rows
   const int lane = tid & 31;
@@ -604,7 +611,7 @@ __device__ __noinline__ void stage_q(const DecodeParams& p, int s, int g, uint32
 #pragma unroll
   for (int i = 0; i < kLoads; ++i) {
     const int f = tid + kN * i, row = f >> 6;
-    qv[i] = row < R ? __ldg(reinterpret_cast<const float4*>(q_row(p, s, g, row)) + (f & 63))
+    qv[i] = row < R ? __ldg(reinterpret_cast<const float4*>(q_row(p, s, g, row0 + row)) + (f & 63))
                     : make_float4(0.f, 0.f, 0.f, 0.f);
   }
 #pragma unroll
@@ -1058,20 +1065,27 @@ __device__ void consume_hg(const DecodeParams& p, uint8_t* smem, uint32_t ring, 
 // second barrier lets every warp form the new maximum, rescale O and its row
 // sums, and scale each warp's P by 2^(base - new).  Row sums are kept per
 // thread over its own keys and reduced once at the end of the piece.
-template <int KT, int VT, int NT>
+template <int KT, int VT, int NT, int kG>
 __device__ void consume_shared(const DecodeParams& p, uint8_t* smem, uint32_t ring, uint32_t bar_full,
                                uint32_t bar_empty, volatile int* abort, long long a, long long b, int s, int g,
-                               int j) {
-  using SM = Smem<KT, VT, NT>;
+                               int j, int grp) {
+  using SM = Smem<KT, VT, NT, kG>;
   using G = StageGeo<KT, VT>;
   constexpr int kStages = SM::kStages;
   constexpr int R8 = NT * 8;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // This group's warps, its query tokens [tok0, tok0 + ntok) and its rows
+  // [row0, row0 + R) of the segment's Rg rows; its own shared memory and
+  // named barrier.
+  const int tid = threadIdx.x & (kCWarps * 32 - 1), warp = tid >> 5, lane = tid & 31;
   const int gq = lane >> 2, tq = lane & 3;
-  const int R = kGqa * p.n_qtok;
-  const uint32_t pb_base = ring + SM::kP;
-  float* mbase = reinterpret_cast<float*>(smem + SM::kStat);             // [2][warp][R8] per-row P base
-  int* flags = reinterpret_cast<int*>(smem + SM::kStat + 2 * kCWarps * R8 * 4);  // [2][warp]
+  const int ntok0 = (p.n_qtok + kG - 1) / kG;
+  const int tok0 = grp * ntok0, ntok = grp == 0 ? ntok0 : p.n_qtok - ntok0;
+  const int R = kGqa * ntok, row0 = kGqa * tok0, Rg = kGqa * p.n_qtok;
+  const uint32_t bar_id = 1 + grp;
+  const int goff = grp * SM::kGrpBytes;
+  const uint32_t pb_base = ring + SM::kP + goff;
+  float* mbase = reinterpret_cast<float*>(smem + SM::kStat + goff);             // [2][warp][R8] per-row P base
+  int* flags = reinterpret_cast<int*>(smem + SM::kStat + goff + 2 * kCWarps * R8 * 4);  // [2][warp]
   // K row group `warp` and V row group 0 of stage 0, with this lane's offsets.
   const uint32_t kg0 = ring + warp * G::kKGroup, vs0 = ring + G::kKBytes;
   const uint32_t kq0 = kg0 + Fmt<KT>::kScales + lane_chunk_offset<KT>(lane);
@@ -1087,10 +1101,10 @@ __device__ void consume_shared(const DecodeParams& p, uint8_t* smem, uint32_t ri
     const int jb = j, je = (int)((long long)ntl < j + (b - x) ? (long long)ntl : j + (b - x));
     const int seg = s * p.segs_per_seq + g;
     const bool whole = (jb == 0 && je == ntl);
-    const uint32_t qf = ring + SM::kQ + qbuf * SM::kQBuf;
-    float* cb4 = reinterpret_cast<float*>(smem + SM::kCb + qbuf * SM::kCbBuf);
-    stage_q<KT, NT>(p, s, g, qf, cb4, tid);
-    named_bar_sync(1, kCWarps * 32);
+    const uint32_t qf = ring + SM::kQ + goff + qbuf * SM::kQBuf;
+    float* cb4 = reinterpret_cast<float*>(smem + SM::kCb + goff + qbuf * SM::kCbBuf);
+    stage_q<KT, NT>(p, s, g, qf, cb4, tid, row0, R);
+    named_bar_sync(bar_id, kCWarps * 32);
     const uint32_t qf_lane = qf + lane * 16;
     const uint32_t cb_lane = smem_u32(cb4) + 16 * tq;
 
@@ -1107,7 +1121,7 @@ __device__ void consume_shared(const DecodeParams& p, uint8_t* smem, uint32_t ri
 #pragma unroll
       for (int e = 0; e < 2; ++e) { m_ref[nt][e] = -INFINITY; l_part[nt][e] = 0.f; }
 
-    const int vis0 = L - p.n_qtok;  // last key visible to query token 0
+    const int vis0 = L - p.n_qtok + tok0;  // last key visible to this group's first token
     for (int jt = jb; jt < je; ++jt) {
       mbar_wait(bar_full + 8 * st, ph, p.err, abort);
       const uint32_t so = st * SM::kStageBytes;
@@ -1131,7 +1145,7 @@ __device__ void consume_shared(const DecodeParams& p, uint8_t* smem, uint32_t ri
           xv[nt][c] *= scale_log2;
           if (need_mask) {
             const int row = nt * 8 + 2 * tq + (c & 1);
-            const int tk = min(row / kGqa, p.n_qtok - 1);
+            const int tk = min(row / kGqa, ntok - 1);
             if (key0 + ((c & 2) ? 8 : 0) > vis0 + tk) xv[nt][c] = -INFINITY;
           }
           up |= xv[nt][c] > m_ref[nt][c & 1] + kLazy;
@@ -1177,7 +1191,7 @@ __device__ void consume_shared(const DecodeParams& p, uint8_t* smem, uint32_t ri
           mb_w[nt * 8 + 2 * tq + 1] = base[nt][1];
         }
       }
-      named_bar_sync(1, kCWarps * 32);
+      named_bar_sync(bar_id, kCWarps * 32);
       const int4 fl = *reinterpret_cast<const int4*>(flags + tbuf * kCWarps);
       const bool any_raise = (fl.x | fl.y | fl.z | fl.w) != 0;  // the same in every warp
 
@@ -1252,7 +1266,7 @@ __device__ void consume_shared(const DecodeParams& p, uint8_t* smem, uint32_t ri
         for (int off = 4; off < 32; off <<= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
         if (gq == 0) lsum[warp * R8 + nt * 8 + 2 * tq + e] = v;
       }
-    named_bar_sync(1, kCWarps * 32);
+    named_bar_sync(bar_id, kCWarps * 32);
     const int slot = (int)blockIdx.x + seg;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -1263,17 +1277,17 @@ __device__ void consume_shared(const DecodeParams& p, uint8_t* smem, uint32_t ri
         float lr = 0.f;
 #pragma unroll
         for (int w2 = 0; w2 < kCWarps; ++w2) lr += lsum[w2 * R8 + row];
-        float* dst = row_dst(p, whole, slot, s, g, row, R);
+        float* dst = row_dst(p, whole, slot, s, g, row0 + row, Rg);
         const float inv = whole ? (lr > 0.f ? 1.f / lr : 0.f) : 1.f;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           dst[vdim<VT>(gq, 4 * warp + i, 0)] = o[i][nt][c] * inv;
           dst[vdim<VT>(gq, 4 * warp + i, 1)] = o[i][nt][2 + c] * inv;
         }
-        if (warp == 0 && gq == 0) write_row_stats(p, whole, slot, s, g, row, R, m_ref[nt][c], lr);
+        if (warp == 0 && gq == 0) write_row_stats(p, whole, slot, s, g, row0 + row, Rg, m_ref[nt][c], lr);
       }
     }
-    named_bar_sync(1, kCWarps * 32);  // lsum is read before the next piece's tiles reuse it
+    named_bar_sync(bar_id, kCWarps * 32);  // lsum is read before the next piece's tiles reuse it
 
     x += je - jb;
     qbuf ^= 1;
@@ -1284,10 +1298,10 @@ __device__ void consume_shared(const DecodeParams& p, uint8_t* smem, uint32_t ri
 
 // ------------------------------------------------------------------ the split kernel
 
-template <int KT, int VT, int NT>
-__global__ void __launch_bounds__(kThreads, CtaTarget<KT, VT, NT>::kN)
+template <int KT, int VT, int NT, int kG>
+__global__ void __launch_bounds__(threads_of(kG), CtaTarget<KT, VT, NT, kG>::kN)
     pa_split_decode_kernel(const __grid_constant__ DecodeParams p) {
-  using SM = Smem<KT, VT, NT>;
+  using SM = Smem<KT, VT, NT, kG>;
   constexpr int kStages = SM::kStages;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   // Align the ring (the chunk addressing needs kAlign); the launch asks for
@@ -1315,7 +1329,7 @@ __global__ void __launch_bounds__(kThreads, CtaTarget<KT, VT, NT>::kN)
     *abort = 0;
     for (int i = 0; i < kStages; ++i) {
       mbar_init(bar_full + 8 * i, 1);
-      mbar_init(bar_empty + 8 * i, NT == 1 ? p.seg_heads : kCWarps);  // one arrival per consuming warp
+      mbar_init(bar_empty + 8 * i, NT == 1 ? p.seg_heads : kCWarps * kG);  // one arrival per consuming warp
     }
     fence_mbar_init();
     int s0, g0, j0;
@@ -1327,7 +1341,7 @@ __global__ void __launch_bounds__(kThreads, CtaTarget<KT, VT, NT>::kN)
   __syncthreads();
   const int s = start[0], g = start[1], j = start[2];
 
-  if (warp == kCWarps) {
+  if (warp == kCWarps * kG) {
     TilePos pos;
     pos.s = s;
     pos.g = g;
@@ -1337,7 +1351,7 @@ __global__ void __launch_bounds__(kThreads, CtaTarget<KT, VT, NT>::kN)
     if constexpr (NT == 1) {
       produce_hg<KT, VT, NT>(p, ring, bar_full, bar_empty, abort, a, b, pos);
     } else {
-      produce_head<KT, VT, NT>(p, ring, bar_full, bar_empty, abort, a, b, pos);
+      produce_head<KT, VT, NT, kG>(p, ring, bar_full, bar_empty, abort, a, b, pos);
     }
     return;
   }
@@ -1345,7 +1359,7 @@ __global__ void __launch_bounds__(kThreads, CtaTarget<KT, VT, NT>::kN)
     if (warp >= p.seg_heads) return;  // a head group smaller than the warp count
     consume_hg<KT, VT>(p, smem, ring, bar_full, bar_empty, abort, a, b, s, g, j);
   } else {
-    consume_shared<KT, VT, NT>(p, smem, ring, bar_full, bar_empty, abort, a, b, s, g, j);
+    consume_shared<KT, VT, NT, kG>(p, smem, ring, bar_full, bar_empty, abort, a, b, s, g, j, warp / kCWarps);
   }
 }
 
@@ -1357,11 +1371,13 @@ struct KernelInfo {
   KernelFn fn;
   int smem;
   int ctas_per_sm_target;
+  int threads;
 };
 
-template <int KT, int VT, int NT>
+template <int KT, int VT, int NT, int kG = 1>
 KernelInfo kernel_info() {
-  return KernelInfo{pa_split_decode_kernel<KT, VT, NT>, Smem<KT, VT, NT>::kLaunch, CtaTarget<KT, VT, NT>::kN};
+  return KernelInfo{pa_split_decode_kernel<KT, VT, NT, kG>, Smem<KT, VT, NT, kG>::kLaunch,
+                    CtaTarget<KT, VT, NT, kG>::kN, threads_of(kG)};
 }
 
 // Defined once per (K, V) format pair, named by the pa_type numbers

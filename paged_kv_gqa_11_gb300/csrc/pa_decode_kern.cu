@@ -2,7 +2,8 @@
 // time with -DPA_KT=<pa_type> -DPA_VT=<pa_type>; the build compiles this file
 // once per pair, so the nine pairs compile in parallel.  Each unit defines
 // lookup_kernel_<K>_<V>, returning the kernel for 1 to 6 n-tiles of 8 query
-// rows (6 rows per token: 1, 2, 3-4, 5, 6, 7-8 tokens).
+// rows (6 rows per token: 1, 2, 3-4, 5, 6, 7-8 tokens); 6 to 8 tokens share
+// one kernel with two consumer groups.
 #include "pa_decode_impl.cuh"
 
 #if !defined(PA_KT) || !defined(PA_VT)
@@ -20,8 +21,11 @@ bool PA_LOOKUP_NAME(PA_KT, PA_VT)(int nt, KernelInfo* out) {
     case 2: *out = kernel_info<PA_KT, PA_VT, 2>(); return true;
     case 3: *out = kernel_info<PA_KT, PA_VT, 3>(); return true;
     case 4: *out = kernel_info<PA_KT, PA_VT, 4>(); return true;
-    case 5: *out = kernel_info<PA_KT, PA_VT, 5>(); return true;
-    case 6: *out = kernel_info<PA_KT, PA_VT, 6>(); return true;
+    // six to eight tokens: two groups of consumer warps, each taking three or
+    // four tokens (three n-tiles); measured faster than one group of five or
+    // six n-tiles, which five tokens keep
+    case 5:
+    case 6: *out = kernel_info<PA_KT, PA_VT, 3, 2>(); return true;
     default: return false;
   }
 }
