@@ -44,7 +44,9 @@
 // against a reference maximum per row that the four warps share (raised, in
 // a rare second step, only when a logit passes it by 2^8), publishes P
 // (transposed with movmatrix) in shared memory, and after a named barrier
-// computes O^T for dims 64w..64w+63 over all 64 keys.
+// computes O^T for dims 64w..64w+63 over all 64 keys.  Six to eight tokens run
+// two such groups of four warps in one CTA, each taking half of the tokens,
+// over the same stage ring.
 //
 // Dequantisation.  K goes into the MMA as raw magic-biased halves: a Q4_0
 // nibble n becomes 1024+n (low) or 1024+16n (high nibble, against Q/16), a
@@ -1057,14 +1059,16 @@ __device__ void consume_hg(const DecodeParams& p, uint8_t* smem, uint32_t ring, 
 
 // ------------------------------------------------------------------ per-head consumer
 
-// Multi-token path (NT = 2, 3): see the file comment.  The four warps share
-// one reference maximum per query row (m_ref), so in the common case a tile
-// needs one barrier and no rescaling: each warp computes P for its 16 keys
-// against m_ref and publishes it.  A warp whose logits exceed m_ref by more
-// than 2^8 raises a flag and publishes its per-row base; then (rarely) a
-// second barrier lets every warp form the new maximum, rescale O and its row
-// sums, and scale each warp's P by 2^(base - new).  Row sums are kept per
-// thread over its own keys and reduced once at the end of the piece.
+// Multi-token path (NT = 2 to 4 n-tiles; with kG = 2 groups, each group of
+// four warps runs this for its half of the query tokens): see the file
+// comment.  The four warps of a group share one reference maximum per query
+// row (m_ref), so in the common case a tile needs one barrier and no
+// rescaling: each warp computes P for its 16 keys against m_ref and publishes
+// it.  A warp whose logits exceed m_ref by more than 2^8 raises a flag and
+// publishes its per-row base; then (rarely) a second barrier lets every warp
+// form the new maximum, rescale O and its row sums, and scale each warp's P by
+// 2^(base - new).  Row sums are kept per thread over its own keys and reduced
+// once at the end of the piece.
 template <int KT, int VT, int NT, int kG>
 __device__ void consume_shared(const DecodeParams& p, uint8_t* smem, uint32_t ring, uint32_t bar_full,
                                uint32_t bar_empty, volatile int* abort, long long a, long long b, int s, int g,
