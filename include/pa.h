@@ -233,9 +233,15 @@ pa_status pa_append_rows_f16(const pa_pool* pool, void* k_pool, void* v_pool, co
  * block_table:  device int32 [n_seq][table_stride]; only entries for pages
  *               holding positions < seq_lens[s] are read.
  * seq_lens_dev / seq_lens_host: the same int32 [n_seq] lengths on the device
- *               and on the host (the host copy sizes the launch).  Each
- *               length must be >= n_qtok and <= table_stride * page_size
- *               (PA_ERR_INVALID otherwise).
+ *               and on the host.  Each host length must be >= n_qtok and
+ *               <= table_stride * page_size (PA_ERR_INVALID otherwise).  The
+ *               host copy alone sizes the launch and drives every read: the
+ *               kernels walk tiles, read table entries and mask keys from it
+ *               (it travels in the launch parameters).  The device copy is
+ *               only compared with it: a sequence whose device length differs
+ *               (whatever its value) gives out = 0 and lse = -inf for all its
+ *               rows and sets *err = PA_ERR_BOUNDS (lucebox PR #555,
+ *               Validation: corrupt bounds must be caught, not followed).
  * out:          device fp32 [n_seq][n_qtok][n_q_heads][head_dim], 16-byte aligned.
  * lse:          device fp32 [n_seq][n_qtok][n_q_heads], or NULL.
  * workspace:    device scratch of ws_bytes >= pa_decode_workspace_size(),
@@ -252,7 +258,9 @@ pa_status pa_append_rows_f16(const pa_pool* pool, void* k_pool, void* v_pool, co
  * Launches: the split kernel, then (when a sequence is split) the merge
  * kernel, on `stream`.  Both are programmatic dependent launches: each may
  * start while the previous kernel on the stream finishes, but waits for it to
- * complete before reading anything, so stream order is kept. */
+ * complete before reading anything, so stream order is kept.  One launch pair
+ * takes at most 128 sequences; a larger batch runs as consecutive sub-batches
+ * of 128 (in order, sharing the workspace), each planned on its own lengths. */
 pa_status pa_decode(const pa_pool* pool, const float* q, const void* k_pool, const void* v_pool,
                     const int32_t* block_table, uint32_t table_stride, const int32_t* seq_lens_dev,
                     const int32_t* seq_lens_host, uint32_t n_seq, uint32_t n_qtok,
@@ -265,7 +273,8 @@ pa_status pa_decode(const pa_pool* pool, const float* q, const void* k_pool, con
  * pa_decode_merge then merges those partials into out/lse.  Calling split then
  * merge on one stream, with the same arguments and workspace and nothing in
  * between that touches the workspace, is exactly pa_decode; the split lets a
- * caller time or schedule the passes separately. */
+ * caller time or schedule the passes separately.  Both take at most 128
+ * sequences (PA_ERR_UNSUPPORTED above that, nothing launched). */
 pa_status pa_decode_split(const pa_pool* pool, const float* q, const void* k_pool, const void* v_pool,
                           const int32_t* block_table, uint32_t table_stride, const int32_t* seq_lens_dev,
                           const int32_t* seq_lens_host, uint32_t n_seq, uint32_t n_qtok, uint32_t n_q_heads,
@@ -284,9 +293,13 @@ pa_status pa_decode_merge(const pa_pool* pool, const float* q, const void* k_poo
  * commit).  0 for an unsupported shape. */
 size_t pa_decode_workspace_size(const pa_pool* pool, uint32_t n_seq, uint32_t n_qtok, int device);
 
-/* How pa_decode would split this batch: *n_ctas decode CTAs, *n_tiles key
- * tiles of `*tile_keys` keys each in total, and *n_partials split partials.
- * Host only; for tests and tools. */
+/* How pa_decode would split this batch (lucebox PR #555, Summary: the
+ * context is split across the GPU by occupancy, adaptively for long
+ * contexts): *n_ctas decode CTAs (the largest grid over the sub-batches),
+ * *n_tiles key tiles of `*tile_keys` keys each in total, and *n_partials
+ * split partials (pieces).  Host only, nothing launched; for tests and tools.
+ * PA_ERR_INVALID for a null pool or lengths, n_seq = 0 or a length below
+ * n_qtok; PA_ERR_UNSUPPORTED for a shape pa_decode does not take. */
 pa_status pa_decode_plan(const pa_pool* pool, const int32_t* seq_lens_host, uint32_t n_seq,
                          uint32_t n_qtok, int device, uint32_t* n_ctas, uint32_t* n_tiles,
                          uint32_t* tile_keys, uint32_t* n_partials);
@@ -318,11 +331,18 @@ pa_status pa_decode_noalloc(const pa_pool* pool, const float* q, const void* k_p
 
 /* ------------------------------------------------------------------ errors */
 
-/* Synchronise `stream`, read the device error word, reset it to 0 and return
- * it as a pa_status (PA_ERR_CUDA if the read itself fails). */
+/* Device-detected failures are reported, not trapped (lucebox PR #555,
+ * Validation: bad block-table bounds are guarded against; llama.cpp fork
+ * PR #2, SDMA copy commit: a stalled wait fails instead of hanging).  The
+ * kernels record the first failure in the caller's int32 word.
+ *
+ * pa_get_error: synchronise `stream`, read the device error word, reset it
+ * to 0 and return it as a pa_status.  PA_ERR_INVALID for a null word,
+ * PA_ERR_CUDA if the read itself fails or the word holds no status. */
 pa_status pa_get_error(int32_t* err, pa_stream_t stream);
 
-/* Static, human-readable name of a status. */
+/* Static, human-readable name of a status (the same failure classes; a
+ * value outside pa_status gives "PA_ERR_UNKNOWN").  Never NULL. */
 const char* pa_status_string(pa_status s);
 
 /* Runs one kernel that waits, with the same bounded wait the decode kernel

@@ -54,11 +54,26 @@ struct MergeTask {
   int seg, c0, np, splits, first_item;
 };
 
-struct MergeParams {
-  DecodeParams p;
-  int n_tasks;
-  MergeTask task[kMaxTasks];
+// What the merge reads of a decode call.
+struct MergeCore {
+  const float2* part_ml;
+  const float* part_o;
+  float* out;
+  float* lse;
+  int n_qtok, n_q_heads, seg_heads, segs_per_seq, rows_per_seg;
 };
+
+// The task list travels in the launch parameters; the kernel is compiled for
+// a few list capacities and the launch takes the smallest that holds the
+// call's tasks, so a batch with a handful of split segments does not ship a
+// 20 KB parameter block.
+template <int kCap>
+struct MergeParams {
+  MergeCore p;
+  int n_tasks;
+  MergeTask task[kCap];
+};
+constexpr int kMergeCaps[3] = {16, 128, kMaxTasks};
 
 // Dim splits for a segment of np pieces: the fewest for which a thread holds
 // at most kMaxPerThread pieces (4 * splits piece groups).
@@ -68,8 +83,9 @@ __host__ __device__ constexpr int merge_splits(int np) {
   return sp;
 }
 
-__global__ void __launch_bounds__(kMergeThreads) pa_merge_kernel(const __grid_constant__ MergeParams mp) {
-  const DecodeParams& p = mp.p;
+template <int kCap>
+__global__ void __launch_bounds__(kMergeThreads) pa_merge_kernel(const __grid_constant__ MergeParams<kCap> mp) {
+  const MergeCore& p = mp.p;
   __shared__ float red_m[kMergeWarps];
   __shared__ float4 part[kMergeThreads];
   __shared__ float red_w[kMergeThreads];
@@ -321,7 +337,10 @@ extern "C" size_t pa_decode_workspace_size(const pa_pool* pool, uint32_t n_seq, 
   int sms = 0, occ = 0;
   if (device_caps(device, d.k_type, d.v_type, nt, ki, &sms, &occ) != PA_OK) return 0;
   const Geometry geo = geometry(d, n_qtok);
-  return workspace_bytes((long long)sms * occ, (long long)n_seq * geo.segs_per_seq, geo.rows_per_seg);
+  // One launch takes at most kInlineSeqs sequences; larger batches reuse the
+  // workspace sub-batch after sub-batch.
+  const long long seqs = std::min<long long>(n_seq, kInlineSeqs);
+  return workspace_bytes((long long)sms * occ, seqs * geo.segs_per_seq, geo.rows_per_seg);
 }
 
 static pa_status make_plan(const pa_pool_desc& d, const int32_t* seq_lens_host, uint32_t n_seq, uint32_t n_qtok,
@@ -360,34 +379,42 @@ extern "C" pa_status pa_decode_plan(const pa_pool* pool, const int32_t* seq_lens
   pa_pool_get_desc(pool, &d);
   if (d.head_dim != kD || n_qtok < 1 || n_qtok > kMaxQTok) return PA_ERR_UNSUPPORTED;
   if (n_seq == 0) return PA_ERR_INVALID;
-  KernelInfo ki;
-  Plan plan{};
-  const pa_status st = make_plan(d, seq_lens_host, n_seq, n_qtok, 0, device, &ki, &plan);
-  if (st != PA_OK) return st;
-  const Geometry& geo = plan.geo;
-  if (n_ctas) *n_ctas = (uint32_t)plan.ctas;
-  if (n_tiles) *n_tiles = (uint32_t)plan.tiles;
-  if (tile_keys) *tile_keys = (uint32_t)geo.tile_keys;
-  if (n_partials) {
+  // Sub-batches of up to kInlineSeqs sequences: the largest grid, and the
+  // tiles and partials summed over the sub-batches.
+  uint32_t ctas = 0, tiles = 0, keys = 0, pieces = 0;
+  for (uint32_t c0 = 0; c0 < n_seq; c0 += kInlineSeqs) {
+    const uint32_t cn = std::min<uint32_t>(kInlineSeqs, n_seq - c0);
+    const int32_t* lens = seq_lens_host + c0;
+    KernelInfo ki;
+    Plan plan{};
+    const pa_status st = make_plan(d, lens, cn, n_qtok, 0, device, &ki, &plan);
+    if (st != PA_OK) return st;
+    const Geometry& geo = plan.geo;
+    ctas = std::max<uint32_t>(ctas, (uint32_t)plan.ctas);
+    tiles += (uint32_t)plan.tiles;
+    keys = (uint32_t)geo.tile_keys;
     // Pieces = CTA-range cuts plus segment cuts.
-    uint32_t pieces = 0;
     long long base = 0;
-    for (uint32_t s = 0; s < n_seq; ++s) {
-      const long long ntl = (seq_lens_host[s] + geo.tile_keys - 1) / geo.tile_keys;
+    for (uint32_t s = 0; s < cn; ++s) {
+      const long long ntl = (lens[s] + geo.tile_keys - 1) / geo.tile_keys;
       for (int g = 0; g < geo.segs_per_seq; ++g) {
         const long long a = base + g * ntl, e = a + ntl - 1;
-        const int c0 = (int)(((a + 1) * plan.ctas - 1) / plan.tiles);
-        const int c1 = (int)(((e + 1) * plan.ctas - 1) / plan.tiles);
-        pieces += (uint32_t)(c1 - c0 + 1);
+        const int c0p = (int)(((a + 1) * plan.ctas - 1) / plan.tiles);
+        const int c1p = (int)(((e + 1) * plan.ctas - 1) / plan.tiles);
+        pieces += (uint32_t)(c1p - c0p + 1);
       }
       base += ntl * geo.segs_per_seq;
     }
-    *n_partials = pieces;
   }
+  if (n_ctas) *n_ctas = ctas;
+  if (n_tiles) *n_tiles = tiles;
+  if (tile_keys) *tile_keys = keys;
+  if (n_partials) *n_partials = pieces;
   return PA_OK;
 }
 
-// Validate a decode call and fill its kernel parameters and launch shape.
+// Validate a decode call of at most kInlineSeqs sequences and fill its kernel
+// parameters and launch shape.
 static pa_status prepare_decode(const pa_pool* pool, const float* q, const void* k_pool, const void* v_pool,
                                 const int32_t* block_table, uint32_t table_stride, const int32_t* seq_lens_dev,
                                 const int32_t* seq_lens_host, uint32_t n_seq, uint32_t n_qtok, uint32_t n_q_heads,
@@ -396,6 +423,7 @@ static pa_status prepare_decode(const pa_pool* pool, const float* q, const void*
   pa_pool_desc d;
   pa_status st = check_shape(pool, n_qtok, n_q_heads, &d);
   if (st != PA_OK) return st;
+  if (n_seq > (uint32_t)kInlineSeqs) return PA_ERR_INVALID;
   if (!q || !k_pool || !v_pool || !block_table || !seq_lens_dev || !seq_lens_host || !out || !workspace || !err ||
       table_stride == 0)
     return PA_ERR_INVALID;
@@ -442,6 +470,7 @@ static pa_status prepare_decode(const pa_pool* pool, const float* q, const void*
   p.segs_per_seq = plan->geo.segs_per_seq;
   p.rows_per_seg = plan->geo.rows_per_seg;
   p.scale_log2 = scale * kLog2e;
+  for (uint32_t i = 0; i < n_seq; ++i) p.lens[i] = seq_lens_host[i];
   return PA_OK;
 }
 
@@ -454,11 +483,29 @@ static pa_status prepare_decode(const pa_pool* pool, const float* q, const void*
   pool, q, k_pool, v_pool, block_table, table_stride, seq_lens_dev, seq_lens_host, n_seq, n_qtok, n_q_heads, \
       scale, out, lse, workspace, ws_bytes, err
 
-static pa_status run_decode(int passes, PA_DECODE_ARGS) {
-  if (n_seq == 0) {
-    pa_pool_desc d;
-    return check_shape(pool, n_qtok, n_q_heads, &d);
-  }
+// Launch the merge with the smallest task-list capacity that holds the call's
+// tasks.
+template <int kCap>
+static pa_status launch_merge(const DecodeParams& p, const Plan& plan, const int32_t* seq_lens_host, uint32_t n_seq,
+                              cudaStream_t cs) {
+  static thread_local MergeParams<kCap> mp;  // up to 20 KB: kept off the stack
+  mp.p = MergeCore{p.part_ml, p.part_o, p.out, p.lse, p.n_qtok, p.n_q_heads, p.seg_heads, p.segs_per_seq,
+                   p.rows_per_seg};
+  mp.n_tasks = list_merge_tasks(seq_lens_host, n_seq, plan.geo, plan.tiles, plan.ctas, mp.task, nullptr);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)plan.merge_items);
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.stream = cs;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, pa_merge_kernel<kCap>, mp) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+// One launch pair over at most kInlineSeqs sequences.
+static pa_status run_chunk(int passes, PA_DECODE_ARGS) {
   DecodeParams p;
   KernelInfo ki;
   Plan plan{};
@@ -482,19 +529,41 @@ static pa_status run_decode(int passes, PA_DECODE_ARGS) {
     if (cudaLaunchKernelEx(&cfg, ki.fn, p) != cudaSuccess) return PA_ERR_CUDA;
   }
   if ((passes & 2) && plan.merge_tasks > 0) {
-    static thread_local MergeParams mp;  // 20 KB: kept off the stack
-    mp.p = p;
-    mp.n_tasks = list_merge_tasks(seq_lens_host, n_seq, plan.geo, plan.tiles, plan.ctas, mp.task, nullptr);
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)plan.merge_items);
-    cfg.blockDim = dim3(kMergeThreads);
-    cfg.stream = cs;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, pa_merge_kernel, mp) != cudaSuccess) return PA_ERR_CUDA;
+    if (plan.merge_tasks <= kMergeCaps[0]) return launch_merge<kMergeCaps[0]>(p, plan, seq_lens_host, n_seq, cs);
+    if (plan.merge_tasks <= kMergeCaps[1]) return launch_merge<kMergeCaps[1]>(p, plan, seq_lens_host, n_seq, cs);
+    return launch_merge<kMergeCaps[2]>(p, plan, seq_lens_host, n_seq, cs);
+  }
+  return PA_OK;
+}
+
+// Batches of more than kInlineSeqs sequences run as consecutive sub-batches
+// that share the workspace; each sub-batch's split kernel waits for the
+// previous sub-batch's kernels (programmatic dependent launch), so stream
+// order is kept.  The separate split / merge passes take one sub-batch only.
+static pa_status run_decode(int passes, PA_DECODE_ARGS) {
+  if (n_seq == 0) {
+    pa_pool_desc d;
+    return check_shape(pool, n_qtok, n_q_heads, &d);
+  }
+  if (n_seq <= (uint32_t)kInlineSeqs) return run_chunk(passes, PA_DECODE_FWD, stream);
+  if (passes != 3) return PA_ERR_UNSUPPORTED;
+  if (!q || !block_table || !seq_lens_dev || !seq_lens_host || !out) return PA_ERR_INVALID;
+  // Check every sub-batch before the first launch, so that a bad length in a
+  // late sub-batch launches nothing.
+  pa_pool_desc d;
+  pa_status st = check_shape(pool, n_qtok, n_q_heads, &d);
+  if (st != PA_OK) return st;
+  for (uint32_t i = 0; i < n_seq; ++i) {
+    const long long L = seq_lens_host[i];
+    if (L < (long long)n_qtok || L > (long long)table_stride * d.page_size) return PA_ERR_INVALID;
+  }
+  const size_t row = (size_t)n_qtok * n_q_heads;  // query rows per sequence
+  for (uint32_t c0 = 0; c0 < n_seq; c0 += kInlineSeqs) {
+    const uint32_t cn = std::min<uint32_t>(kInlineSeqs, n_seq - c0);
+    st = run_chunk(passes, pool, q + c0 * row * kD, k_pool, v_pool, block_table + (size_t)c0 * table_stride,
+                   table_stride, seq_lens_dev + c0, seq_lens_host + c0, cn, n_qtok, n_q_heads, scale,
+                   out + c0 * row * kD, lse ? lse + c0 * row : nullptr, workspace, ws_bytes, err, stream);
+    if (st != PA_OK) return st;
   }
   return PA_OK;
 }

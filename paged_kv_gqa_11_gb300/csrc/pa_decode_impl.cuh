@@ -92,6 +92,9 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLazy = 8.0f;  // log2 headroom before the running max is raised
 constexpr int kAlign = 512;    // stage-ring alignment the chunk addressing relies on
+// Sequences one launch takes: their host lengths travel in the kernel
+// parameters, and larger batches run as consecutive sub-batches.
+constexpr int kInlineSeqs = 128;
 
 // ------------------------------------------------------------------ stage geometry
 
@@ -240,6 +243,12 @@ struct DecodeParams {
   int segs_per_seq;  // n_kv_heads / seg_heads
   int rows_per_seg;  // query rows per segment: 6 * seg_heads * n_qtok
   float scale_log2;  // scale * log2(e)
+  // The host copy of the lengths (n_seq <= kInlineSeqs).  The tile walk, the
+  // table reads and the masks use only these, so nothing the device copy
+  // holds can move a read out of a sequence's table row; seq_lens (device) is
+  // only compared with them, and a sequence whose two copies differ gives
+  // zeros (lse -inf) and PA_ERR_BOUNDS.
+  int lens[kInlineSeqs];
 };
 
 // Shared-memory layout (byte offsets from the kAlign-aligned base).
@@ -278,7 +287,7 @@ __device__ __forceinline__ int tiles_of(const DecodeParams& p, int L) { return (
 __device__ __forceinline__ void locate_tile(const DecodeParams& p, long long x, int& s_out, int& g_out, int& j_out) {
   long long base = 0;
   for (int s = 0; s < p.n_seq; ++s) {
-    const long long nt = tiles_of(p, p.seq_lens[s]);
+    const long long nt = tiles_of(p, p.lens[s]);
     const long long span = nt * p.segs_per_seq;
     if (x < base + span) {
       const long long r = x - base;
@@ -306,7 +315,7 @@ __device__ __forceinline__ void next_tile(const DecodeParams& p, TilePos& t) {
   if (++t.g < p.segs_per_seq) return;
   t.g = 0;
   if (++t.s < p.n_seq) {
-    t.L = p.seq_lens[t.s];
+    t.L = p.lens[t.s];
     t.nt = tiles_of(p, t.L);
   }
 }
@@ -891,6 +900,13 @@ __device__ __forceinline__ void zero_tail_tile(uint32_t vstage, int n, int w, in
   __syncwarp();
 }
 
+// ------------------------------------------------------------------ device lengths
+
+// The device copy of sequence s's length, read past L1 (the caller may have
+// written it just before the launch).  Issued when a piece starts and checked
+// when it ends, so its latency hides behind the piece's tiles.
+__device__ __forceinline__ int device_len(const DecodeParams& p, int s) { return __ldcg(p.seq_lens + s); }
+
 // ------------------------------------------------------------------ piece output
 
 // Write one query row's result: the final output (out = O / l, lse) when the
@@ -942,7 +958,8 @@ __device__ void consume_hg(const DecodeParams& p, uint8_t* smem, uint32_t ring, 
   uint32_t ph = 0;
   long long x = a;
   while (x < b) {
-    const int L = p.seq_lens[s];
+    const int L = p.lens[s];
+    const int l_dev = device_len(p, s);
     const int ntl = tiles_of(p, L);
     const int jb = j, je = (int)((long long)ntl < j + (b - x) ? (long long)ntl : j + (b - x));
     const int seg = s * p.segs_per_seq + g;
@@ -1021,6 +1038,14 @@ __device__ void consume_hg(const DecodeParams& p, uint8_t* smem, uint32_t ring, 
       ls0 += __shfl_xor_sync(0xffffffffu, ls0, off);
       ls1 += __shfl_xor_sync(0xffffffffu, ls1, off);
     }
+    // A device length that differs from the host's: the piece counts for
+    // nothing (zeros, l = 0) and the mismatch is reported.
+    const float keep = (l_dev == L) ? 1.f : 0.f;
+    if (l_dev != L) {
+      if (lane == 0) record_error(p.err, PA_ERR_BOUNDS);
+      ls0 = 0.f;
+      ls1 = 0.f;
+    }
     const int slot = (int)blockIdx.x + seg;
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
@@ -1029,7 +1054,7 @@ __device__ void consume_hg(const DecodeParams& p, uint8_t* smem, uint32_t ring, 
       const float lr = c ? ls1 : ls0, mr = c ? mref1 : mref0;
       const int row = warp * kGqa + hl;  // row within the segment
       float* dst;
-      float inv = 1.f;
+      float inv = keep;
       if (whole) {
         dst = p.out + ((long long)s * p.n_q_heads + head * kGqa + hl) * kD;
         inv = lr > 0.f ? 1.f / lr : 0.f;
@@ -1100,7 +1125,8 @@ __device__ void consume_shared(const DecodeParams& p, uint8_t* smem, uint32_t ri
   int qbuf = 0, tbuf = 0;
   long long x = a;
   while (x < b) {
-    const int L = p.seq_lens[s];
+    const int L = p.lens[s];
+    const int l_dev = device_len(p, s);
     const int ntl = tiles_of(p, L);
     const int jb = j, je = (int)((long long)ntl < j + (b - x) ? (long long)ntl : j + (b - x));
     const int seg = s * p.segs_per_seq + g;
@@ -1271,6 +1297,10 @@ __device__ void consume_shared(const DecodeParams& p, uint8_t* smem, uint32_t ri
         if (gq == 0) lsum[warp * R8 + nt * 8 + 2 * tq + e] = v;
       }
     named_bar_sync(bar_id, kCWarps * 32);
+    // A device length that differs from the host's: the piece counts for
+    // nothing (zeros, l = 0) and the mismatch is reported.
+    const bool len_ok = l_dev == L;
+    if (!len_ok && tid == 0) record_error(p.err, PA_ERR_BOUNDS);
     const int slot = (int)blockIdx.x + seg;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -1281,8 +1311,9 @@ __device__ void consume_shared(const DecodeParams& p, uint8_t* smem, uint32_t ri
         float lr = 0.f;
 #pragma unroll
         for (int w2 = 0; w2 < kCWarps; ++w2) lr += lsum[w2 * R8 + row];
+        if (!len_ok) lr = 0.f;
         float* dst = row_dst(p, whole, slot, s, g, row0 + row, Rg);
-        const float inv = whole ? (lr > 0.f ? 1.f / lr : 0.f) : 1.f;
+        const float inv = whole ? (lr > 0.f ? 1.f / lr : 0.f) : (len_ok ? 1.f : 0.f);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           dst[vdim<VT>(gq, 4 * warp + i, 0)] = o[i][nt][c] * inv;
@@ -1344,13 +1375,14 @@ __global__ void __launch_bounds__(threads_of(kG), CtaTarget<KT, VT, NT, kG>::kN)
   }
   __syncthreads();
   const int s = start[0], g = start[1], j = start[2];
+  if (s >= p.n_seq) return;  // an empty range (the planner gives every CTA a tile)
 
   if (warp == kCWarps * kG) {
     TilePos pos;
     pos.s = s;
     pos.g = g;
     pos.j = j;
-    pos.L = p.seq_lens[s];
+    pos.L = p.lens[s];
     pos.nt = tiles_of(p, pos.L);
     if constexpr (NT == 1) {
       produce_hg<KT, VT, NT>(p, ring, bar_full, bar_empty, abort, a, b, pos);

@@ -99,13 +99,6 @@ def test_config2_uniform():
     assert_lse_close(gl, ol, what="config2")
 
 
-def _sampled(w, pairs):
-    sel = np.zeros((w.n_seq, W.HQ), bool)
-    for s, h in pairs:
-        sel[s, h] = True
-    return sel
-
-
 @pytest.fixture(scope="module")
 def ragged():
     w = W.config(3)
@@ -114,13 +107,12 @@ def ragged():
     return w, go, gl
 
 
-def test_config3_ragged_sampled(ragged):
+def test_config3_ragged_full(ragged):
+    """Every (sequence, query head) row of the ragged batch."""
     w, go, gl = ragged
-    pairs = [(0, 0), (0, 7), (0, 23), (3, 12), (7, 5)]
-    oo, ol = oracle.decode_workload(w, n_threads=THREADS, select=_sampled(w, pairs))
-    for s, h in pairs:
-        assert_close(go[s, :, h], oo[s, :, h], what=f"config3 s{s} h{h}")
-        assert_lse_close(gl[s, :, h], ol[s, :, h], what=f"config3 s{s} h{h}")
+    oo, ol = oracle.decode_workload(w, n_threads=THREADS)
+    assert_close(go, oo, what="config3")
+    assert_lse_close(gl, ol, what="config3")
 
 
 def test_config3_paged_equals_contiguous(ragged):
@@ -152,36 +144,28 @@ def test_page_size_invariance_and_repeats():
 @pytest.mark.parametrize("nq", [1, 2, 3, 4, 5, 6, 7, 8])
 def test_config4_verify(nq):
     """The verify workload at one to four tokens, and at five to eight (the
-    wider verify batches the fork's decode kernel later took)."""
+    wider verify batches the fork's decode kernel later took); every row."""
     w = W.config(4, n_qtok=nq)
     go, gl = run_decode(w)
-    sel = _sampled(w, [(s, h) for s in range(4) for h in (0, 5, 6, 17, 23)])
-    oo, ol = oracle.decode_workload(w, n_threads=THREADS, select=sel)
-    for s in range(4):
-        for h in (0, 5, 6, 17, 23):
-            assert_close(go[s, :, h], oo[s, :, h], what=f"config4 nq{nq} s{s} h{h}")
-            assert_lse_close(gl[s, :, h], ol[s, :, h], what=f"config4 nq{nq} s{s} h{h}")
+    oo, ol = oracle.decode_workload(w, n_threads=THREADS)
+    assert_close(go, oo, what=f"config4 nq{nq}")
+    assert_lse_close(gl, ol, what=f"config4 nq{nq}")
 
 
-def test_config5a_long_f16_sampled():
+def test_config5a_long_f16_full():
     w = W.config(5, variant="a")
     go, gl = run_decode(w)
-    pairs = [(0, 0), (0, 11), (0, 23)]
-    oo, ol = oracle.decode_workload(w, n_threads=THREADS, select=_sampled(w, pairs))
-    for s, h in pairs:
-        assert_close(go[s, :, h], oo[s, :, h], what=f"config5a h{h}")
-        assert_lse_close(gl[s, :, h], ol[s, :, h], what=f"config5a h{h}")
+    oo, ol = oracle.decode_workload(w, n_threads=THREADS)
+    assert_close(go, oo, what="config5a")
+    assert_lse_close(gl, ol, what="config5a")
 
 
-def test_config5b_many_sampled():
+def test_config5b_many_full():
     w = W.config(5, variant="b")
     go, gl = run_decode(w)
-    longest = int(np.argmax(w.seq_lens))
-    pairs = [(longest, 3), (0, 0), (17, 9), (40, 22), (63, 14)]
-    oo, ol = oracle.decode_workload(w, n_threads=THREADS, select=_sampled(w, pairs))
-    for s, h in pairs:
-        assert_close(go[s, :, h], oo[s, :, h], what=f"config5b s{s} h{h}")
-        assert_lse_close(gl[s, :, h], ol[s, :, h], what=f"config5b s{s} h{h}")
+    oo, ol = oracle.decode_workload(w, n_threads=THREADS)
+    assert_close(go, oo, what="config5b")
+    assert_lse_close(gl, ol, what="config5b")
 
 
 def test_fully_masked_split_is_finite():
@@ -233,6 +217,63 @@ def test_bounds_guard_reports_and_stays_finite():
     # sequence 1 does not touch the bad entry: still exact
     oo, _ = oracle.decode_workload(w)
     assert_close(out.cpu().numpy()[1], oo[1], what="unaffected sequence")
+
+
+@pytest.mark.parametrize("nq", [1, 3])
+def test_device_lengths_are_checked(nq):
+    """The decode walks the host copy of the lengths; a device length that
+    differs from it (longer by a page, past the table's capacity, negative,
+    shorter by one key) gives zeros and lse -inf for that sequence and
+    PA_ERR_BOUNDS, and reads nothing outside the sequence's table row (lucebox
+    PR #555, Validation: guards against corrupt block-table bounds).  The
+    other sequences stay exact; the long one is split over many CTAs."""
+    w = W.make_workload("lenguard", 61, [300, 80, 1000], 16, Q8, Q8, nq, "shuffled")
+    cache, tab = device_cache(w)
+    oo, ol = oracle.decode_workload(w)
+    cap = tab.shape[1] * w.page_size
+    q = to_dev(w.q)
+    for bad_s, bad_len in ((0, 316), (2, 1 << 30), (1, -5), (1, 79), (2, cap + 16)):
+        dev = w.seq_lens.copy()
+        dev[bad_s] = bad_len
+        out, lse = cache.decode(q, tab, to_dev(dev), w.seq_lens, nq, w.scale)
+        torch.cuda.synchronize()
+        assert cache.check() == PA_ERR_BOUNDS, (bad_s, bad_len)
+        o, l = out.cpu().numpy(), lse.cpu().numpy()
+        assert (o[bad_s] == 0).all() and np.isneginf(l[bad_s]).all(), (bad_s, bad_len)
+        for s in range(w.n_seq):
+            if s != bad_s:
+                assert_close(o[s], oo[s], what=f"unaffected sequence {s}")
+                assert_lse_close(l[s], ol[s], what=f"unaffected sequence {s}")
+    # and the same call with agreeing lengths is clean
+    out, lse = cache.decode(q, tab, to_dev(w.seq_lens), w.seq_lens, nq, w.scale)
+    torch.cuda.synchronize()
+    assert cache.check() == PA_OK
+    assert_close(out.cpu().numpy(), oo, what="agreeing lengths")
+
+
+def test_large_batch_runs_in_sub_batches():
+    """More sequences than one launch takes (128): the library runs
+    consecutive sub-batches that share the workspace; the result matches the
+    oracle and a repeat is bit-identical.  The separate split / merge passes
+    refuse such a batch."""
+    rng = np.random.default_rng(41)
+    lens = rng.integers(3, 400, size=300).astype(np.int32)
+    lens[7] = 5000
+    w = W.make_workload("subbatch", 41, lens, 16, Q4, Q8, 3, "shuffled")
+    cache, tab = device_cache(w)
+    go, gl = run_decode(w, cache, tab)
+    oo, ol = oracle.decode_workload(w, n_threads=THREADS)
+    assert_close(go, oo, what="sub-batches")
+    assert_lse_close(gl, ol, what="sub-batches")
+    go2, gl2 = run_decode(w, cache, tab)
+    assert np.array_equal(go, go2) and np.array_equal(gl, gl2)
+    from paged_kv_gqa_11_gb300 import PA_ERR_UNSUPPORTED, pa_decode
+    q, sl = to_dev(w.q), to_dev(w.seq_lens)
+    out = torch.empty_like(q)
+    ws = cache.workspace(w.n_seq, w.n_qtok)
+    rc = pa_decode(cache.pool, q, cache.k_pool, cache.v_pool, tab, tab.shape[1], sl, w.seq_lens, w.n_seq, 3, W.HQ,
+                   w.scale, out, None, ws, ws.numel(), cache.err, check=False, passes="split")
+    assert rc == PA_ERR_UNSUPPORTED
 
 
 def test_bounded_wait_expires_with_status():
@@ -317,17 +358,15 @@ def test_prefix_fork_with_copy_on_write():
     assert pool.release(hA[:6] + [hB6, hB7]) == PA_OK and pool.free_count() == free0 + 2
 
 
-def test_shared_prefix_batch_sampled():
-    """Eight sequences sharing a 32K-row prompt's pages: sampled heads match
-    the oracle, and sharing leaves results equal to a private copy of the
-    prefix (the contiguous layout)."""
+def test_shared_prefix_batch_full():
+    """Eight sequences sharing a prompt's pages: every row matches the oracle,
+    and sharing leaves results equal to a private copy of the prefix (the
+    contiguous layout)."""
     w = W.shared_prefix(n_seq=8, prefix=4096, own=300)
     go, gl = run_decode(w)
-    pairs = [(0, 0), (1, 9), (4, 17), (7, 23)]
-    oo, ol = oracle.decode_workload(w, n_threads=THREADS, select=_sampled(w, pairs))
-    for s, h in pairs:
-        assert_close(go[s, :, h], oo[s, :, h], what=f"shared s{s} h{h}")
-        assert_lse_close(gl[s, :, h], ol[s, :, h], what=f"shared s{s} h{h}")
+    oo, ol = oracle.decode_workload(w, n_threads=THREADS)
+    assert_close(go, oo, what="shared prefix")
+    assert_lse_close(gl, ol, what="shared prefix")
     co, cl = run_decode(w.contiguous())
     assert np.array_equal(go, co) and np.array_equal(gl, cl)
 
