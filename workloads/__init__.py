@@ -206,6 +206,24 @@ class Workload:
                         self.k_type, self.v_type, self.table, self.k_rows, self.v_rows, q,
                         self.scale, dict(self.meta))
 
+    def subset(self, seq_ids) -> "Workload":
+        """The batch made of sequences seq_ids (in that order, repeats
+        allowed): their rows, queries and pages.  Block numbers are renumbered
+        compactly, keeping their relative order (so the placement pattern
+        survives); a repeated sequence gets its own copy of its pages."""
+        ids = [int(i) for i in seq_ids]
+        offs = self.seq_offsets
+        lens = self.seq_lens[ids].astype(np.int32)
+        k_rows = np.concatenate([self.k_rows[offs[i]:offs[i + 1]] for i in ids]) if ids else self.k_rows[:0]
+        v_rows = np.concatenate([self.v_rows[offs[i]:offs[i + 1]] for i in ids]) if ids else self.v_rows[:0]
+        pages = [self.table[i, :pages_needed(self.seq_lens[i], self.page_size)] for i in ids]
+        keys = sorted((int(b), n, j) for n, pg in enumerate(pages) for j, b in enumerate(pg))
+        new = {(n, j): r for r, (_, n, j) in enumerate(keys)}
+        lists = [[new[(n, j)] for j in range(len(pg))] for n, pg in enumerate(pages)]
+        return Workload(self.name, lens, self.n_qtok, self.page_size, len(keys), self.k_type, self.v_type,
+                        table_from_lists(lists), k_rows, v_rows, np.ascontiguousarray(self.q[ids]), self.scale,
+                        dict(self.meta))
+
     def contiguous(self, slots_per_seq: int | None = None) -> "Workload":
         """Same rows through an identity table: sequence s owns blocks
         [s*P, (s+1)*P) in order, P = slots_per_seq / page_size."""
@@ -346,6 +364,83 @@ def percall(length: int, n_qtok: int) -> Workload:
     assert length in PERCALL_LENGTHS and n_qtok in (1, 3, 4)
     return make_workload(f"percall-{ {32768: 32, 131072: 131, 262144: 262}[length]}k-{n_qtok}", 6, [length], 256, TYPE_Q8_0, TYPE_Q4_0,
                          n_qtok, "shuffled")
+
+
+def _table_for(rng: np.random.Generator, lengths, ps: int, layout: str):
+    """Block table of `lengths` for the 'interleaved' / 'shuffled' / 'identity'
+    layouts of make_workload; returns (table, n_blocks)."""
+    lists = interleaved_blocks(lengths, ps)
+    n_pages = sum(len(l) for l in lists)
+    if layout == "shuffled":
+        perm = rng.permutation(n_pages)
+        lists = [[int(perm[b]) for b in l] for l in lists]
+    elif layout == "identity":
+        nxt, lists = 0, []
+        for L in lengths:
+            n = pages_needed(L, ps)
+            lists.append(list(range(nxt, nxt + n)))
+            nxt += n
+    elif layout != "interleaved":
+        raise ValueError(layout)
+    return table_from_lists(lists), n_pages
+
+
+STRESS_KINDS = ("rising", "late", "bigq", "scales")
+
+
+def stress_workload(kind: str, seed: int, lengths, ps: int, k_type: int, v_type: int, n_qtok: int,
+                    layout: str = "shuffled") -> Workload:
+    """Inputs that push the online softmax's running maximum up after the
+    first keys of a sequence, so that a decoder must rescale an accumulator
+    that already holds weight (plus blocks with zero and subnormal scales).
+    Only the K / V sources and Q are shaped; they are then stored exactly as
+    make_workload stores them.
+
+    kind 'rising': each KV head's key sources drift towards the last query
+        token's first query head of its group, K_j = N(0,1) + 3 (j+1)/L q,
+        so that head's logits grow along the sequence (to about 48) and the
+        others' spread grows with it.
+    kind 'late':   N(0,1) keys except two dominant ones, 2 q at 0.8 L and
+        1.5 q at 0.55 L (q as above), far past the first tiles; the pieces of
+        a split sequence then carry maxima tens of units apart.
+    kind 'bigq':   N(0,1) K/V and Q = 16 N(0,1) rounded to binary16 values
+        (so Q itself carries no rounding): logits of standard deviation 16.
+    kind 'scales': N(0,1) K/V sources whose 32-value blocks are, at random,
+        zero (scale 0), multiplied by 2^-14 (binary16 scales and values in the
+        subnormal range) or left as they are; Q as in 'rising'.
+    """
+    assert kind in STRESS_KINDS, kind
+    rng = np.random.default_rng(seed)
+    lengths = np.asarray(lengths, dtype=np.int32)
+    table, n_blocks = _table_for(rng, lengths, ps, layout)
+    q = rng.standard_normal((len(lengths), n_qtok, HQ, D), dtype=np.float32)
+    if kind == "bigq":
+        q = (q * np.float32(16.0)).astype(np.float16).astype(np.float32)
+    ks, vs = [], []
+    for s, L in enumerate(lengths.tolist()):
+        qhat = q[s, n_qtok - 1, ::GQA, :]  # [HKV][D]: the first query head of each group
+        for a in range(0, L, _GEN_CHUNK):
+            b = min(L, a + _GEN_CHUNK)
+            xk = rng.standard_normal((b - a, HKV, D), dtype=np.float32)
+            xv = rng.standard_normal((b - a, HKV, D), dtype=np.float32)
+            if kind == "rising":
+                ramp = (np.arange(a, b, dtype=np.float32) + 1) * np.float32(3.0 / L)
+                xk += ramp[:, None, None] * qhat[None]
+            elif kind == "late":
+                for pos, c in ((int(0.8 * L), 2.0), (int(0.55 * L), 1.5)):
+                    if a <= pos < b and L > 64:
+                        xk[pos - a] = np.float32(c) * qhat
+            elif kind == "scales":
+                for x in (xk, xv):
+                    cat = rng.integers(0, 5, size=(b - a, HKV, D // 32))
+                    f = np.where(cat == 0, np.float32(0.0), np.where(cat == 1, np.float32(2.0 ** -14), np.float32(1.0)))
+                    x *= np.repeat(f, 32, axis=2).astype(np.float32)
+            ks.append(encode_rows(xk, k_type))
+            vs.append(encode_rows(xv, v_type))
+    k_rows = np.concatenate(ks) if ks else np.zeros((0, HKV, row_bytes(k_type)), np.uint8)
+    v_rows = np.concatenate(vs) if vs else np.zeros((0, HKV, row_bytes(v_type)), np.uint8)
+    return Workload(f"stress-{kind}", lengths, n_qtok, ps, n_blocks, k_type, v_type, table, k_rows, v_rows, q,
+                    SCALE, {"seed": seed, "layout": layout, "stress": kind})
 
 
 def small_workload(seed: int, lengths, ps: int, k_type: int, v_type: int | None = None,
