@@ -7,17 +7,22 @@ Workload (default): the ragged eight-request decode of lucebox PR #555
 requests arrived together, Q4_0 K/V from N(0,1) sources, D=256, 24 query heads
 on 4 KV heads, one query token.  Synthetic, seeded inputs.
 
-One step = one pa_decode (split-K pass + merge pass) over the whole batch.
-Metric: K/V GB/s = algorithmic K+V bytes read per step (every live row of
-every KV head once) / step time, and us/step.  L2 is flushed (a 2 x L2 write)
-between timed steps, outside the timed region.
+One step = one pa_decode (split-K pass + merge pass) over the whole batch,
+replayed from a CUDA graph.  Metric: K/V GB/s = algorithmic K+V bytes read per
+step (every live row of every KV head once) / step time, and us/step.  Between
+timed steps L2 is flushed outside the timed region: a buffer of twice the L2
+is written and then read back, so that neither the inputs nor dirty lines of
+the flush are left in L2 when a step starts.  The same steps without the flush
+("warm") are reported beside them.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-Multi-GPU (torchrun): every rank decodes its own copy of the batch, with no
-data-path communication (the (sequence, KV head) segments are independent);
-the value is the bytes all ranks processed over the slowest rank's time.
---impl reference times the float64 CPU oracle on the host cores instead.
+Multi-GPU (torchrun): the global batch is N copies of the workload's sequences,
+partitioned across the ranks by sequence with the K/V bytes balanced
+(partition.py), with no data-path communication (the (sequence, KV head)
+segments are independent); the value is the bytes all ranks processed over the
+slowest rank's time.  --impl reference times the float64 CPU oracle on the
+host cores instead.
 """
 from __future__ import annotations
 
@@ -43,7 +48,7 @@ FALLBACK_HBM_GBS = 6800.0
 # RTX 3090, paged, same workload: 4.095 ms per step (lucebox PR #555, ragged
 # table) = 217,055,232 B / 4.095 ms = 53.0 GB/s.  Another machine: context.
 PAGES_PAGED_3090_MS = 4.095
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_split_ragged_q4_0.md")
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
 DECODE_SOURCES = ["paged_kv_gqa_11_gb300/csrc/pa_decode.cu", "paged_kv_gqa_11_gb300/csrc/pa_decode_impl.cuh",
                   "paged_kv_gqa_11_gb300/csrc/pa_decode_kern.cu", "paged_kv_gqa_11_gb300/csrc/pa_device.cuh",
                   "paged_kv_gqa_11_gb300/csrc/pa_layout.cuh"]
@@ -93,25 +98,21 @@ def source_hash() -> str:
 
 
 def profile_traffic(workload: str):
-    """DRAM bytes per launch of the split kernel from the committed ncu summary,
-    if it was taken on this workload with the current kernel source."""
+    """DRAM bytes per launch of the split kernel (dram__bytes_read.sum +
+    dram__bytes_write.sum from one ncu capture), from profiles/traffic.json,
+    if it was taken on this workload with the current kernel sources."""
     try:
-        text = open(PROFILE_SUMMARY).read()
-    except OSError:
+        with open(PROFILE_TRAFFIC) as f:
+            entries = json.load(f)
+    except (OSError, ValueError):
         return None
-    vals = {}
-    for line in text.splitlines():
-        if line.startswith("traffic:"):
-            for kv in line[len("traffic:"):].split(";"):
-                if "=" in kv:
-                    k, v = kv.split("=", 1)
-                    vals[k.strip()] = v.strip()
-    if vals.get("source") != source_hash() or vals.get("workload") != workload:
-        return None
-    try:
-        return int(vals["bytes_per_launch"])
-    except (KeyError, ValueError):
-        return None
+    for e in entries if isinstance(entries, list) else []:
+        if e.get("workload") == workload and e.get("source") == source_hash():
+            try:
+                return int(e["dram_bytes_per_launch"])
+            except (KeyError, TypeError, ValueError):
+                return None
+    return None
 
 
 def measured_peaks():
@@ -123,34 +124,44 @@ def measured_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle samples while the timed region runs."""
+    """nvidia-smi clock / throttle samples over the GPU phase of the run.
+
+    The window opens before the warm-up and closes after the last GPU leg, so
+    that a short run still holds samples under load; the samples inside the
+    headline timed region are counted separately."""
 
     FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int, period_ms: int = 20):
+    def __init__(self, gpu_index: int, period_ms: int = 10):
         self.gpu = gpu_index
         self.period = period_ms
         self.proc = None
         self.lines = []
         self.t_begin = self.t_end = None
+        self.timed = []  # (begin, end) of the headline timed regions
+
+    @staticmethod
+    def _now():
+        from datetime import datetime
+        return datetime.now()
 
     def begin(self):
-        """Mark the start of the timed region (samples before it are ignored)."""
-        from datetime import datetime
-        self.t_begin = datetime.now()
+        self.t_begin = self._now()
 
     def end(self):
-        from datetime import datetime
-        self.t_end = datetime.now()
+        self.t_end = self._now()
         time.sleep(3 * self.period / 1000.0)
+
+    def mark_timed(self, t0, t1):
+        self.timed.append((t0, t1))
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 f"-lms", str(self.period)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", str(self.period)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self._t = threading.Thread(target=self._read, daemon=True)
             self._t.start()
             time.sleep(0.3)  # let the first samples arrive
@@ -171,10 +182,10 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         from datetime import datetime
-        for ln in self.lines:
+        sm, mx, reasons, in_timed = [], [], set(), 0
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in list(self.lines):
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -189,13 +200,15 @@ class ClockSampler:
                 mx.append(float(parts[2]))
             except ValueError:
                 continue
+            in_timed += any(a <= ts <= b for a, b in self.timed)
             for name, v in zip(names, parts[5:9]):
                 if v.lower() == "active":
                     reasons.add(name)
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "samples_in_timed_region": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "sm_mhz_min": min(sm),
+                "reasons": sorted(reasons), "samples": len(sm), "samples_in_timed_region": in_timed,
+                "window": "warm-up to the last GPU leg, every 10 ms"}
 
 
 def rank_max(dist, x: float, device) -> float:
@@ -339,6 +352,22 @@ def run_append(args, w: W.Workload):
                      "frac": round(gbps / peak, 4), "traffic": None}}))
 
 
+def percentiles(ms):
+    a = np.sort(np.asarray(ms, dtype=np.float64))
+    return {"mean_us": round(float(a.mean()) * 1e3, 2), "median_us": round(float(np.median(a)) * 1e3, 2),
+            "p10_us": round(float(np.percentile(a, 10)) * 1e3, 2), "p90_us": round(float(np.percentile(a, 90)) * 1e3, 2)}
+
+
+def rank_workload(w: W.Workload, world: int, rank: int) -> W.Workload:
+    """This rank's share of a global batch of `world` copies of w's
+    sequences, partitioned by sequence with the K/V bytes balanced."""
+    from paged_kv_gqa_11_gb300 import partition
+    n = w.n_seq
+    lens = np.tile(w.seq_lens, world)
+    parts = partition.balance_by_sequence(partition.kv_bytes_per_sequence(lens, w.k_type, w.v_type, W.HKV), world)
+    return w.subset([i % n for i in parts[rank]])
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -372,6 +401,7 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(local)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        w = rank_workload(w, world, rank)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
 
@@ -384,6 +414,7 @@ def main():
         if dist is not None:
             dist.barrier()
 
+    clocks = ClockSampler(local).__enter__()
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
     cache = PagedKVCache(w.n_blocks, w.page_size, w.k_type, w.v_type, device=dev)
     table = t(w.table)
@@ -395,6 +426,14 @@ def main():
         raise SystemExit("append reported a device error")
     kv_bytes = w.kv_bytes()
     plan = pa.pa_decode_plan(cache.pool, sl_host, w.n_qtok, local)
+    # our kernels per step: one split kernel per sub-batch of up to 128
+    # sequences, plus a merge kernel where a segment is split into pieces
+    launches_per_step = 0
+    for c0 in range(0, w.n_seq, 128):
+        sub = sl_host[c0:c0 + 128]
+        pl = pa.pa_decode_plan(cache.pool, sub, w.n_qtok, local)
+        segs = len(sub) * (1 if w.n_qtok == 1 else W.HKV)
+        launches_per_step += 1 + (pl["partials"] > segs)
 
     # Step inputs (query + one new K/V row per sequence + its index) packed in
     # one buffer, outputs (out + lse) in another: one H2D and one D2H per step
@@ -427,55 +466,80 @@ def main():
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush_buf = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+    flush_acc = torch.empty((), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def decode(passes):
-        pa.pa_decode(cache.pool, q, cache.k_pool, cache.v_pool, table, table.shape[1], sl_dev, sl_host, w.n_seq,
-                     w.n_qtok, W.HQ, w.scale, out, lse, ws, ws.numel(), cache.err, stream.cuda_stream,
-                     passes=passes)
-
-    for _ in range(args.warmup):
+    def flush():
+        # write 2 x L2, then read it back: the write evicts the inputs, the
+        # read evicts the flush's own dirty lines (their write-back happens
+        # here, not inside the next timed step)
         flush_buf.fill_(1.0)
-        decode("all")
-    torch.cuda.synchronize()
-    if cache.check() != pa.PA_OK:
-        raise SystemExit("decode reported a device error")
+        torch.sum(flush_buf, dim=0, out=flush_acc)
 
-    # ---- timed steps: one pa_decode (split + merge) each, L2 flushed between
-    K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
-    with ClockSampler(local) as clocks:
+    def decode(passes, s):
+        pa.pa_decode(cache.pool, q, cache.k_pool, cache.v_pool, table, table.shape[1], sl_dev, sl_host, w.n_seq,
+                     w.n_qtok, W.HQ, w.scale, out, lse, ws, ws.numel(), cache.err, s, passes=passes)
+
+    def capture(passes):
+        """pa_decode (or one pass) captured once into a CUDA graph."""
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            decode(passes, side.cuda_stream)
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            decode(passes, side.cuda_stream)
+        torch.cuda.synchronize()
+        return g
+
+    g_all, g_split, g_merge = capture("all"), capture("split"), capture("merge")
+    clock_hz = 2.0e9
+
+    def prime(n_steps):
+        # a bounded device sleep ahead of the timed steps, so that the host
+        # queues them all before the GPU reaches the first one
+        torch.cuda._sleep(int(clock_hz * min(0.1, 1e-3 + 40e-6 * n_steps)))
+
+    def timed(n, body, pre=None, headline=False):
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
         barrier()
         torch.cuda.synchronize()
-        clocks.begin()
-        wall0 = time.perf_counter()
-        for i in range(K):
-            flush_buf.fill_(1.0)
+        t0 = ClockSampler._now()
+        prime(n)
+        for i in range(n):
+            if pre:
+                pre()
             ev[i][0].record(stream)
-            decode("all")
+            body()
             ev[i][1].record(stream)
         torch.cuda.synchronize()
         barrier()
-        wall = time.perf_counter() - wall0
-        clocks.end()
-    my_step = statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in range(K))
+        if headline:
+            clocks.mark_timed(t0, ClockSampler._now())
+        return [ev[i][0].elapsed_time(ev[i][1]) for i in range(n)]
+
+    clocks.begin()
+    for _ in range(args.warmup):
+        flush()
+        g_all.replay()
+    torch.cuda.synchronize()
     if cache.check() != pa.PA_OK:
         raise SystemExit("decode reported a device error")
 
-    # ---- the split kernel alone (the roofline's kernel): split pass timed, merge after it
+    # ---- headline: K graph replays of pa_decode, L2 flushed between
+    K = args.steps
+    wall0 = time.perf_counter()
+    step_ms = timed(K, g_all.replay, flush, headline=True)
+    wall = time.perf_counter() - wall0
+    if cache.check() != pa.PA_OK:
+        raise SystemExit("decode reported a device error")
+    # ---- the same steps back to back, no flush (warm)
+    warm_ms = timed(K, g_all.replay)
+    # ---- the split kernel alone (the roofline's kernel), merge replayed after it
     KS = max(3, min(K, 1000))
-    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(KS)]
-    barrier()
-    torch.cuda.synchronize()
-    for i in range(KS):
-        flush_buf.fill_(1.0)
-        sev[i][0].record(stream)
-        decode("split")
-        sev[i][1].record(stream)
-        decode("merge")
-    torch.cuda.synchronize()
-    barrier()
-    my_split = statistics.mean(sev[i][0].elapsed_time(sev[i][1]) for i in range(KS))
+    split_ms = timed(KS, g_split.replay, lambda: (g_merge.replay(), flush()))
 
     # ---- end to end through the public API: packed host inputs in, host outputs back
     h2d = h_in.numel()
@@ -484,34 +548,27 @@ def main():
     def e2e_step():
         d_in.copy_(h_in, non_blocking=True)
         cache.append(d_k, d_v, d_seq, d_pos, table, stream=stream.cuda_stream)
-        decode("all")
+        decode("all", stream.cuda_stream)
         h_outbuf.copy_(d_outbuf, non_blocking=True)
 
     for _ in range(3):
-        flush_buf.fill_(1.0)
+        flush()
         e2e_step()
     torch.cuda.synchronize()
-    E = args.e2e_steps
-    eev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(E)]
-    barrier()
-    torch.cuda.synchronize()
-    for i in range(E):
-        flush_buf.fill_(1.0)
-        eev[i][0].record(stream)
-        e2e_step()
-        eev[i][1].record(stream)
-    torch.cuda.synchronize()
-    barrier()
-    my_e2e = statistics.mean(eev[i][0].elapsed_time(eev[i][1]) for i in range(E))
+    e2e_ms = timed(args.e2e_steps, e2e_step, flush)
+    clocks.end()
+    clocks.__exit__()
     if cache.check() != pa.PA_OK:
         raise SystemExit("end-to-end step reported a device error")
     if not np.isfinite(h_outbuf.numpy()).all():
         raise SystemExit("non-finite output")
 
     # ---- max over ranks
+    my_step, my_split, my_e2e, my_warm = (statistics.mean(x) for x in (step_ms, split_ms, e2e_ms, warm_ms))
     step = rank_max(dist, my_step, dev)
     split = rank_max(dist, my_split, dev)
     e2e = rank_max(dist, my_e2e, dev)
+    warm = rank_max(dist, my_warm, dev)
     n = world
     value = job_gbps(n, kv_bytes, step)
     achieved = kv_bytes / (split * 1e-3) / 1e9
@@ -525,8 +582,12 @@ def main():
         ocache = oracle_cache(w)
         pairs = oracle_segments(w, ocache, args.cpu_budget, threads)
         secs = oracle_time(w, ocache, pairs, threads)
+        pairs1 = oracle_segments(w, ocache, max(1.0, args.cpu_budget / 3), 1)
+        secs1 = oracle_time(w, ocache, pairs1, 1)
         cpu = {"value": round(sample_bytes(w, pairs) / secs / 1e9, 4), "unit": "GB/s", "cores": threads,
-               "kind": "oracle", "sample": sample_desc(w, pairs) + f"; {secs:.1f} s wall on {threads} threads"}
+               "kind": "oracle", "sample": sample_desc(w, pairs) + f"; {secs:.1f} s wall on {threads} threads",
+               "single_thread": {"value": round(sample_bytes(w, pairs1) / secs1 / 1e9, 4), "unit": "GB/s",
+                                 "cores": 1, "sample": sample_desc(w, pairs1) + f"; {secs1:.1f} s wall"}}
 
     if dist is not None:
         dist.destroy_process_group()
@@ -554,11 +615,15 @@ def main():
             "kv_bytes_per_step": kv_bytes,
             "kv_storage": f"K {W.TYPE_NAMES[w.k_type]} / V {W.TYPE_NAMES[w.v_type]}",
             "arithmetic": "fp16 tensor-core products, fp32 accumulation and softmax",
-            "l2": "flushed (2 x L2 write) between timed steps, outside the timed region",
+            "l2": "flushed between timed steps outside the timed region (2 x L2 written, then read back)",
             "plan": plan,
-            "timing": "CUDA events on the launching stream around each pa_decode (split + merge), mean over steps",
+            "timing": "CUDA events on the launching stream around each CUDA-graph replay of pa_decode "
+                      "(split + merge); value from the mean over the steps",
+            "multi_gpu": f"global batch of {n} copies, partitioned by sequence, K/V bytes balanced" if n > 1 else None,
             "wall_s": round(wall, 3),
         },
+        "timing": {"flushed": percentiles(step_ms), "warm": percentiles(warm_ms),
+                   "warm_gbps": round(job_gbps(n, kv_bytes, warm), 2), "split_kernel": percentiles(split_ms)},
         "frac_of_hbm_peak": round(value / n / peak, 4),
         "roofline": {
             "bound": "hbm",
@@ -572,8 +637,9 @@ def main():
             "split_us": round(split * 1e3, 2),
         },
         "e2e": {"value": round(n * kv_bytes / (e2e * 1e-3) / 1e9, 2), "unit": "GB/s",
-                "us_per_step": round(e2e * 1e3, 2), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 2 * K,  # split + merge kernels per timed step
+                "us_per_step": round(e2e * 1e3, 2), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "path": "pa_append_rows + pa_decode through the C ABI, pinned host buffers, no graph"},
+        "gpu_launches": launches_per_step * K,  # split (+ merge) kernels per sub-batch, per timed step
         "clocks": clocks.summary(),
         "cpu_baseline": cpu,
     }
