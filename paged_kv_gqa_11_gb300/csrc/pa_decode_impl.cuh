@@ -123,13 +123,14 @@ constexpr int extras_bytes(int NT, int kG = 1) {
          + 2 * 8 * 8 + 32;  // barriers (up to 8 stages), misc
 }
 
-// CTAs per SM a configuration aims for: three for small one-token stages,
-// otherwise two, or one when a stage is large.
+// CTAs per SM a configuration aims for: two, or one when a stage is large
+// or the consumers hold many accumulators.  (Three CTAs of the one-token
+// kernel with three stages each stream no faster than two with five, and cut
+// a long sequence into half as many pieces again for the merge to read.)
 template <int KT, int VT, int NT, int kG = 1>
 struct CtaTarget {
   static constexpr int kStageBytes = StageGeo<KT, VT>::kBytes;
-  static constexpr int kN = (NT > 3 || kG > 1) ? 1
-                            : (kStageBytes <= 20000 && NT == 1) ? 3 : (kStageBytes <= 40000 ? 2 : 1);
+  static constexpr int kN = (NT > 3 || kG > 1) ? 1 : (kStageBytes <= 40000 ? 2 : 1);
 };
 
 template <int KT, int VT, int NT, int kG = 1>
@@ -333,32 +334,42 @@ __device__ __forceinline__ uint32_t lane_chunk_offset(int lane) {
 
 // ------------------------------------------------------------------ producers
 
-// A head-group tile's place in the CTA's walk, with its page and first slot
-// kept incrementally (no division per tile).
-struct HgPos {
-  TilePos t;
-  int page, slot0;  // page index within the sequence, first slot of the tile in it
-};
-
-__device__ __forceinline__ HgPos hg_start(const DecodeParams& p, const TilePos& t) {
-  const int k0 = t.j * kTileHG;
-  return HgPos{t, k0 / p.page_size, k0 % p.page_size};
-}
-
-__device__ __forceinline__ void hg_next(const DecodeParams& p, HgPos& h) {
-  const int s = h.t.s, g = h.t.g;
-  next_tile(p, h.t);
-  if (h.t.s != s || h.t.g != g) {
-    h.page = 0;
-    h.slot0 = 0;
-  } else if ((h.slot0 += kTileHG) == p.page_size) {
-    h.slot0 = 0;
-    ++h.page;
+// Move a tile position k >= 0 tiles forward, across segments; past the last
+// sequence it stops at s = n_seq.
+__device__ __forceinline__ void advance_tiles(const DecodeParams& p, TilePos& t, long long k) {
+  while (k > 0 && t.s < p.n_seq) {
+    const long long left = t.nt - t.j;
+    if (k < left) {
+      t.j += (int)k;
+      return;
+    }
+    k -= left;
+    t.j = 0;
+    if (++t.g == p.segs_per_seq) {
+      t.g = 0;
+      if (++t.s < p.n_seq) {
+        t.L = p.lens[t.s];
+        t.nt = tiles_of(p, t.L);
+      }
+    }
   }
 }
 
-__device__ __forceinline__ int hg_table_entry(const DecodeParams& p, const HgPos& h) {
-  return __ldg(p.table + (long long)h.t.s * p.table_stride + h.page);
+// Pool row (K and V pools alike) of the first slot of head-group tile t for
+// the group's first KV head, or -1 when its table entry is outside the pool.
+__device__ __forceinline__ long long hg_tile_row(const DecodeParams& p, const TilePos& t) {
+  const int k0 = t.j * kTileHG;
+  const int tb = __ldg(p.table + (long long)t.s * p.table_stride + k0 / p.page_size);
+  if (!(tb >= 0 && tb < p.n_blocks)) return -1;
+  return ((long long)tb * p.n_kv_heads + (long long)t.g * p.seg_heads) * p.page_size + k0 % p.page_size;
+}
+
+// The producer warp resolves the pool rows of 32 consecutive tiles at once,
+// lane l taking tile w0 + l (one table read per lane, issued together), and
+// the next 32 a window ahead, so that no tile waits on its table read.
+__device__ __forceinline__ long long hg_window(const DecodeParams& p, TilePos t, long long w0, long long b, int lane) {
+  advance_tiles(p, t, lane);
+  return (w0 + lane < b && t.s < p.n_seq) ? hg_tile_row(p, t) : -1;
 }
 
 // Table entry for row group `lane` (0..3) of a per-head tile, -1 past its keys.
@@ -400,19 +411,27 @@ __device__ void produce_hg(const DecodeParams& p, uint32_t ring, uint32_t bar_fu
   int st = 0;
   uint32_t ph = 0;
   long long issued = 0;
-  HgPos cur = hg_start(p, pos);
-  int tb = hg_table_entry(p, cur), tbn = -1;
+  // rows of tiles w0 .. w0+31 (this window) and w0+32 .. w0+63 (the next)
+  long long w0 = a;
+  TilePos wnext = pos;
+  advance_tiles(p, wnext, 32);
+  long long rows = hg_window(p, pos, w0, b, lane);
+  long long rows_next = hg_window(p, wnext, w0 + 32, b, lane);
   for (long long x = a; x < b; ++x) {
     if (*abort) break;
-    HgPos nxt = cur;
-    if (x + 1 < b) {
-      hg_next(p, nxt);
-      tbn = hg_table_entry(p, nxt);
+    int k = (int)(x - w0);
+    if (k == 32) {
+      w0 += 32;
+      k = 0;
+      rows = rows_next;
+      advance_tiles(p, wnext, 32);
+      rows_next = hg_window(p, wnext, w0 + 32, b, lane);
     }
+    const long long row0 = __shfl_sync(0xffffffffu, rows, k);  // this tile's first row, or -1
     const uint32_t fb = bar_full + 8 * st, eb = bar_empty + 8 * st;
     mbar_wait(eb, ph ^ 1, p.err, abort);  // every lane: no divergent branch
     const uint32_t sk = ring + st * G::kBytes, sv = sk + G::kKBytes;
-    if (!(tb >= 0 && tb < p.n_blocks)) {
+    if (row0 < 0) {
       // Outside the pool: zero rows for every head of the group, no copy.
       if (lane == 0) record_error(p.err, PA_ERR_BOUNDS);
       for (int i = lane; i < GH * G::kKGroup / 16; i += 32) sts128_zero(sk + 16 * i);
@@ -420,30 +439,25 @@ __device__ void produce_hg(const DecodeParams& p, uint32_t ring, uint32_t bar_fu
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(fb);
+    } else if (whole_blocks) {
+      if (lane == 0) {
+        mbar_arrive_expect_tx(fb, (uint32_t)H * (G::kKGroup + G::kVGroup));
+        bulk_g2s_hint(sk, p.k_pool + row0 * RK, (uint32_t)H * G::kKGroup, fb, policy);
+        bulk_g2s_hint(sv, p.v_pool + row0 * RV, (uint32_t)H * G::kVGroup, fb, policy);
+      }
+      __syncwarp();
     } else {
-      // First row of the group of head h0 = g * GH.
-      const long long row0 = ((long long)tb * H + cur.t.g * GH) * ps + cur.slot0;
-      if (whole_blocks) {
-        if (lane == 0) {
-          mbar_arrive_expect_tx(fb, (uint32_t)H * (G::kKGroup + G::kVGroup));
-          bulk_g2s_hint(sk, p.k_pool + row0 * RK, (uint32_t)H * G::kKGroup, fb, policy);
-          bulk_g2s_hint(sv, p.v_pool + row0 * RV, (uint32_t)H * G::kVGroup, fb, policy);
-        }
-      } else {
-        if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)GH * (G::kKGroup + G::kVGroup));
-        __syncwarp();
-        if (lane < GH) {
-          const long long row = row0 + (long long)lane * ps;
-          bulk_g2s_hint(sk + lane * G::kKGroup, p.k_pool + row * RK, G::kKGroup, fb, policy);
-          bulk_g2s_hint(sv + lane * G::kVGroup, p.v_pool + row * RV, G::kVGroup, fb, policy);
-        }
+      if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)GH * (G::kKGroup + G::kVGroup));
+      __syncwarp();
+      if (lane < GH) {
+        const long long row = row0 + (long long)lane * ps;
+        bulk_g2s_hint(sk + lane * G::kKGroup, p.k_pool + row * RK, G::kKGroup, fb, policy);
+        bulk_g2s_hint(sv + lane * G::kVGroup, p.v_pool + row * RV, G::kVGroup, fb, policy);
       }
       __syncwarp();
     }
     ++issued;
     if (++st == kStages) { st = 0; ph ^= 1; }
-    cur = nxt;
-    tb = tbn;
   }
   if (lane == 0) drain_ring<kStages>(p, bar_full, abort, st, ph, issued);
 }
