@@ -69,6 +69,9 @@ def workload_for(name: str) -> W.Workload:
         return W.config(5, variant="b")
     if name == "shared-prefix":  # 8 sequences forked from a 32K-token prompt, 1K own rows each
         return W.shared_prefix()
+    if name.startswith("rows-"):  # rows-<4k|16k|64k>-<17|65|96>: row tiles, Q8_0 K / Q4_0 V, one sequence
+        _, size, nq = name.split("-")
+        return W.rows_workload({"4k": 4096, "16k": 16384, "64k": 65536}[size], int(nq))
     if name.startswith("percall-"):  # percall-<32k|131k|262k>-<1|3|4>: Q8_0 K / Q4_0 V, one sequence
         _, size, nq = name.split("-")
         return W.percall({"32k": 32768, "131k": 131072, "262k": 262144}[size], int(nq))
@@ -597,6 +600,10 @@ def main():
         raise SystemExit("non-finite output")
 
     # ---- max over ranks
+    # algorithmic flops of a step: QK^T and PV over every visible key of every
+    # query row (2 x 2 x 256 per key and row)
+    flops = sum(sum(int(L) - w.n_qtok + t + 1 for t in range(w.n_qtok)) for L in w.seq_lens) * W.HQ * W.D * 4
+    tensor_bound = w.n_qtok > 8  # row tiles: flop/B far above the HBM ridge
     my_iso, my_split, my_e2e, my_warm = (statistics.mean(x) for x in (step_ms, split_ms, e2e_ms, warm_ms))
     my_step = pipe_ms[0] if pipelined else my_iso
     step = rank_max(dist, my_step, dev)
@@ -610,6 +617,10 @@ def main():
     peaks = measured_peaks()
     peak = float(peaks["hbm_gbs"]) if peaks and "hbm_gbs" in peaks else FALLBACK_HBM_GBS
     peak_src = "measured (MEASURED_PEAKS.json hbm_gbs, copy)" if peaks else "fallback"
+    # binary16 MMA runs at the bf16 rate; a kernel timed alone takes the burst figure
+    tpeak = float(peaks["bf16_tflops"]) if peaks and "bf16_tflops" in peaks else 1900.0
+    tpeak_src = ("measured (MEASURED_PEAKS.json bf16_tflops, cuBLAS burst; fp16 MMA at the bf16 rate)" if peaks
+                 else "fallback 1.9 PFLOP/s")
 
     cpu = None
     if rank == 0 and n == 1 and not args.no_cpu_baseline:
@@ -668,7 +679,7 @@ def main():
                    "isolated_warm": percentiles(warm_ms), "isolated_warm_gbps": round(job_gbps(n, kv_bytes, warm), 2),
                    "split_kernel_flushed": percentiles(split_ms)},
         "frac_of_hbm_peak": round(value / n / peak, 4),
-        "roofline": {
+        "roofline": ({
             "bound": "hbm",
             "kernel": "pa_split_decode_kernel",
             "achieved": round(achieved, 2),
@@ -678,7 +689,19 @@ def main():
             "traffic": profile_traffic(wl),
             "peak_source": peak_src,
             "split_us": round(split * 1e3, 2),
-        },
+        } if not tensor_bound else {
+            "bound": "tensor",
+            "kernel": "pa_rows_decode_kernel",
+            "achieved": round(flops / (split * 1e-3) / 1e12, 2),
+            "peak": tpeak,
+            "unit": "TFLOP/s",
+            "frac": round(flops / (split * 1e-3) / 1e12 / tpeak, 4),
+            "traffic": profile_traffic(wl),
+            "peak_source": tpeak_src,
+            "split_us": round(split * 1e3, 2),
+            "flops_per_step": flops,
+            "hbm_gbps_of_split": round(achieved, 2),
+        }),
         "e2e": {"value": round(n * kv_bytes / (e2e * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "us_per_step": round(e2e * 1e3, 2), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "path": "pa_append_rows + pa_decode through the C ABI, pinned host buffers, no graph"},

@@ -212,9 +212,13 @@ pa_status pa_append_rows_f16(const pa_pool* pool, void* k_pool, void* v_pool, co
  * Single-step GQA decode attention over a paged cache: split-K flash decoding
  * through a block table, with a log-sum-exp merge of the splits (llama.cpp
  * fork PR #2, split-K decode commit: head size 256, GQA 6, one to four query
- * tokens for speculative verification, and a later commit taking batches of
- * up to eight tokens; lucebox PR #555, Summary: a numerically stable merge
- * of split softmaxes).
+ * tokens for speculative verification, a later commit taking batches of up
+ * to eight tokens, and the commit on ubatches of more than eight tokens, which
+ * gives paged K/V of up to 96 query tokens the decode kernel's row tiles;
+ * lucebox PR #555, Summary: a numerically stable merge of split softmaxes).
+ * One to eight query tokens run the decode kernels; nine to 96 run row tiles
+ * (128 query rows of one KV head, K and V dequantised once per tile into
+ * binary16).
  *
  * For sequence s with L = seq_lens[s] cached rows (the n_qtok new rows
  * included), query token t in [0, n_qtok) sits at position L - n_qtok + t and
@@ -225,7 +229,7 @@ pa_status pa_append_rows_f16(const pa_pool* pool, void* k_pool, void* v_pool, co
  * plus the log of the row sum).  A row with no visible key would give
  * out = 0 and lse = -inf.
  *
- * Supported: head_dim 256, n_q_heads / n_kv_heads = 6, n_qtok 1..8, K and V
+ * Supported: head_dim 256, n_q_heads / n_kv_heads = 6, n_qtok 1..96, K and V
  * each F16, Q4_0 or Q8_0 (PA_ERR_UNSUPPORTED otherwise).
  *
  * q:            device fp32 [n_seq][n_qtok][n_q_heads][head_dim], 16-byte aligned.

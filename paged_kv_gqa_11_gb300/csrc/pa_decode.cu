@@ -19,7 +19,7 @@
 #include <mutex>
 
 #include "pa.h"
-#include "pa_decode_impl.cuh"
+#include "pa_rows_impl.cuh"
 
 using namespace pa_dev;
 using namespace pa_split;
@@ -61,6 +61,7 @@ struct MergeCore {
   float* out;
   float* lse;
   int n_qtok, n_q_heads, seg_heads, segs_per_seq, rows_per_seg;
+  int n_row_tiles;  // row tiles per KV head (9 to 96 tokens), else 0
 };
 
 // The task list travels in the launch parameters; the kernel is compiled for
@@ -179,9 +180,14 @@ __global__ void __launch_bounds__(kMergeThreads) pa_merge_kernel(const __grid_co
     Wt += red_w[w * wcols + col % wcols];
   }
   // Segment row -> output row: a head group's rows are (head, query head) of
-  // one token; a single head's rows are (token, query head).
+  // one token; a single head's rows are (token, query head), and a row tile's
+  // rows continue them from 128 * (row tile).
   long long orow;
-  if (p.seg_heads > 1 || p.n_qtok == 1) {
+  if (p.n_row_tiles > 0) {
+    const int head = g / p.n_row_tiles, rg = kRowTile * (g % p.n_row_tiles) + row;
+    if (rg >= kGqa * p.n_qtok) return;  // a padding row of the last row tile
+    orow = ((long long)s * p.n_qtok + rg / kGqa) * p.n_q_heads + head * kGqa + rg % kGqa;
+  } else if (p.seg_heads > 1 || p.n_qtok == 1) {
     orow = (long long)s * p.n_q_heads + (long long)g * p.seg_heads * kGqa + row;
   } else {
     const int t = row / kGqa, hl = row % kGqa;
@@ -204,14 +210,40 @@ bool lookup_kernel(int kt, int vt, int nt, KernelInfo* out) {
   return false;
 }
 
+bool lookup_rows_kernel(int kt, int vt, KernelInfo* out) {
+#define PA_PAIR(k, v) \
+  if (kt == k && vt == v) return lookup_rows_kernel_##k##_##v(out);
+  PA_PAIR(1, 1) PA_PAIR(1, 2) PA_PAIR(1, 8)
+  PA_PAIR(2, 1) PA_PAIR(2, 2) PA_PAIR(2, 8)
+  PA_PAIR(8, 1) PA_PAIR(8, 2) PA_PAIR(8, 8)
+#undef PA_PAIR
+  return false;
+}
+
+// The split kernel for n_qtok query tokens: the decode kernels up to eight
+// tokens (by n-tiles of 8 query rows), the row-tile kernel from nine to 96.
+// *slot: its index in the occupancy cache.
+bool pick_kernel(int kt, int vt, uint32_t n_qtok, KernelInfo* ki, int* slot) {
+  if (n_qtok >= 1 && n_qtok <= (uint32_t)kMaxQTok) {
+    const int nt = (kGqa * (int)n_qtok + 7) / 8;
+    *slot = nt - 1;
+    return lookup_kernel(kt, vt, nt, ki);
+  }
+  if (n_qtok > (uint32_t)kMaxQTok && n_qtok <= (uint32_t)kMaxRowsQTok) {
+    *slot = kMaxNT;
+    return lookup_rows_kernel(kt, vt, ki);
+  }
+  return false;
+}
+
 int type_slot(int t) { return t == PA_F16 ? 0 : t == PA_Q4_0 ? 1 : t == PA_Q8_0 ? 2 : -1; }
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 int g_sms[kMaxDevices];
-int g_occ[kMaxDevices][3][3][kMaxNT];  // [device][k][v][nt-1] CTAs per SM, 0 = not queried
+int g_occ[kMaxDevices][3][3][kMaxNT + 1];  // [device][k][v][kernel slot] CTAs per SM, 0 = not queried
 
-pa_status device_caps(int device, int kt, int vt, int nt, const KernelInfo& ki, int* sms, int* occ) {
+pa_status device_caps(int device, int kt, int vt, int slot, const KernelInfo& ki, int* sms, int* occ) {
   if (device < 0 || device >= kMaxDevices) return PA_ERR_INVALID;
   std::lock_guard<std::mutex> lk(g_mu);
   if (g_sms[device] == 0) {
@@ -219,7 +251,7 @@ pa_status device_caps(int device, int kt, int vt, int nt, const KernelInfo& ki, 
     if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return PA_ERR_CUDA;
     g_sms[device] = v;
   }
-  int& o = g_occ[device][type_slot(kt)][type_slot(vt)][nt - 1];
+  int& o = g_occ[device][type_slot(kt)][type_slot(vt)][slot];
   if (o == 0) {
     int cur = 0;
     cudaGetDevice(&cur);
@@ -241,21 +273,33 @@ pa_status check_shape(const pa_pool* pool, uint32_t n_qtok, uint32_t n_q_heads, 
   pa_pool_get_desc(pool, d);
   if (d->head_dim != kD) return PA_ERR_UNSUPPORTED;
   if (n_q_heads == 0 || n_q_heads != d->n_kv_heads * kGqa) return PA_ERR_UNSUPPORTED;
-  if (n_qtok < 1 || n_qtok > kMaxQTok) return PA_ERR_UNSUPPORTED;
   KernelInfo ki;
-  if (!lookup_kernel(d->k_type, d->v_type, (kGqa * n_qtok + 7) / 8, &ki)) return PA_ERR_UNSUPPORTED;
+  int slot = 0;
+  if (!pick_kernel(d->k_type, d->v_type, n_qtok, &ki, &slot)) return PA_ERR_UNSUPPORTED;
   return PA_OK;
 }
 
 // Segment geometry for n_qtok query tokens: one token uses head-group tiles
 // (16 keys of up to four KV heads; the group is the largest of 4, 3, 2, 1 that
-// divides the KV head count), more tokens use per-head tiles of 64 keys.
+// divides the KV head count), two to eight tokens per-head tiles of 64 keys,
+// and nine to 96 tokens row tiles (segments of 128 query rows of one KV head,
+// 64-key tiles).
 struct Geometry {
   int tile_keys, seg_heads, segs_per_seq, rows_per_seg;
+  int n_row_tiles;  // row tiles per KV head, or 0
 };
 
 Geometry geometry(const pa_pool_desc& d, uint32_t n_qtok) {
   Geometry g;
+  g.n_row_tiles = 0;
+  if (n_qtok > (uint32_t)kMaxQTok) {
+    g.tile_keys = kTile;
+    g.seg_heads = 1;
+    g.n_row_tiles = (kGqa * (int)n_qtok + kRowTile - 1) / kRowTile;
+    g.segs_per_seq = (int)d.n_kv_heads * g.n_row_tiles;
+    g.rows_per_seg = kRowTile;
+    return g;
+  }
   if (n_qtok == 1) {
     int gh = 1;
     for (int c = kCWarps; c >= 1; --c)
@@ -271,6 +315,16 @@ Geometry geometry(const pa_pool_desc& d, uint32_t n_qtok) {
   return g;
 }
 
+// Tiles of segment gi of a sequence of length L (the device side's
+// tiles_of / row_seg_tiles): a row tile takes the 64-key tiles its last row
+// sees.
+long long seg_tiles(const Geometry& geo, long long L, uint32_t n_qtok, int gi) {
+  if (geo.n_row_tiles == 0) return (L + geo.tile_keys - 1) / geo.tile_keys;
+  const int rt = gi % geo.n_row_tiles;
+  const long long t_last = std::min<long long>(n_qtok - 1, (kRowTile * (rt + 1) - 1) / kGqa);
+  return (L - n_qtok + t_last + 1 + geo.tile_keys - 1) / geo.tile_keys;
+}
+
 struct Plan {
   Geometry geo;
   long long tiles;
@@ -284,15 +338,16 @@ struct Plan {
 // List the merge tasks (every segment with more than one piece) into task[];
 // returns their number, or -1 past kMaxTasks.  *n_items gets the number of
 // work items (CTAs of the merge grid).
-int list_merge_tasks(const int32_t* seq_lens_host, uint32_t n_seq, const Geometry& geo, long long tiles, int ctas,
-                     MergeTask* task, long long* n_items) {
+int list_merge_tasks(const int32_t* seq_lens_host, uint32_t n_seq, uint32_t n_qtok, const Geometry& geo,
+                     long long tiles, int ctas, MergeTask* task, long long* n_items) {
   int n = 0;
   long long items = 0;
   long long base = 0;
   for (uint32_t s = 0; s < n_seq; ++s) {
-    const long long ntl = (seq_lens_host[s] + geo.tile_keys - 1) / geo.tile_keys;
     for (int g = 0; g < geo.segs_per_seq; ++g) {
-      const long long a = base + g * ntl, e = a + ntl - 1;
+      const long long ntl = seg_tiles(geo, seq_lens_host[s], n_qtok, g);
+      const long long a = base, e = a + ntl - 1;
+      base += ntl;
       const int c0 = (int)(((a + 1) * ctas - 1) / tiles), c1 = (int)(((e + 1) * ctas - 1) / tiles);
       const int np = c1 - c0 + 1;
       if (np < 2) continue;
@@ -302,7 +357,6 @@ int list_merge_tasks(const int32_t* seq_lens_host, uint32_t n_seq, const Geometr
       items += (long long)sp * geo.rows_per_seg;
       ++n;
     }
-    base += ntl * geo.segs_per_seq;
   }
   if (n_items) *n_items = items;
   return n;
@@ -330,12 +384,12 @@ size_t workspace_bytes(long long max_ctas, long long n_seg, int R) { return work
 extern "C" size_t pa_decode_workspace_size(const pa_pool* pool, uint32_t n_seq, uint32_t n_qtok, int device) {
   pa_pool_desc d;
   if (pa_pool_get_desc(pool, &d) != PA_OK) return 0;
-  if (d.head_dim != kD || n_qtok < 1 || n_qtok > kMaxQTok) return 0;
-  const int nt = (kGqa * (int)n_qtok + 7) / 8;
+  if (d.head_dim != kD) return 0;
   KernelInfo ki;
-  if (!lookup_kernel(d.k_type, d.v_type, nt, &ki)) return 0;
+  int slot = 0;
+  if (!pick_kernel(d.k_type, d.v_type, n_qtok, &ki, &slot)) return 0;
   int sms = 0, occ = 0;
-  if (device_caps(device, d.k_type, d.v_type, nt, ki, &sms, &occ) != PA_OK) return 0;
+  if (device_caps(device, d.k_type, d.v_type, slot, ki, &sms, &occ) != PA_OK) return 0;
   const Geometry geo = geometry(d, n_qtok);
   // One launch takes at most kInlineSeqs sequences; larger batches reuse the
   // workspace sub-batch after sub-batch.
@@ -345,19 +399,18 @@ extern "C" size_t pa_decode_workspace_size(const pa_pool* pool, uint32_t n_seq, 
 
 static pa_status make_plan(const pa_pool_desc& d, const int32_t* seq_lens_host, uint32_t n_seq, uint32_t n_qtok,
                            uint32_t table_stride, int device, KernelInfo* ki, Plan* plan) {
-  const int nt = (kGqa * (int)n_qtok + 7) / 8;
-  if (!lookup_kernel(d.k_type, d.v_type, nt, ki)) return PA_ERR_UNSUPPORTED;
+  int slot = 0;
+  if (!pick_kernel(d.k_type, d.v_type, n_qtok, ki, &slot)) return PA_ERR_UNSUPPORTED;
   const Geometry geo = geometry(d, n_qtok);
   long long tiles = 0;
   for (uint32_t s = 0; s < n_seq; ++s) {
     const long long L = seq_lens_host[s];
     if (L < (long long)n_qtok) return PA_ERR_INVALID;
     if (table_stride && L > (long long)table_stride * d.page_size) return PA_ERR_INVALID;
-    tiles += (L + geo.tile_keys - 1) / geo.tile_keys;
+    for (int g = 0; g < geo.segs_per_seq; ++g) tiles += seg_tiles(geo, L, n_qtok, g);
   }
-  tiles *= geo.segs_per_seq;
   int sms = 0, occ = 0;
-  pa_status st = device_caps(device, d.k_type, d.v_type, nt, *ki, &sms, &occ);
+  pa_status st = device_caps(device, d.k_type, d.v_type, slot, *ki, &sms, &occ);
   if (st != PA_OK) return st;
   plan->geo = geo;
   plan->tiles = tiles;
@@ -366,7 +419,8 @@ static pa_status make_plan(const pa_pool_desc& d, const int32_t* seq_lens_host, 
   plan->slots = (long long)plan->ctas + plan->n_seg;
   // Each multi-piece segment holds a CTA boundary, so there are fewer merge
   // tasks than CTAs: kMaxTasks covers any grid of up to 1024 CTAs.
-  plan->merge_tasks = list_merge_tasks(seq_lens_host, n_seq, geo, tiles, plan->ctas, nullptr, &plan->merge_items);
+  plan->merge_tasks =
+      list_merge_tasks(seq_lens_host, n_seq, n_qtok, geo, tiles, plan->ctas, nullptr, &plan->merge_items);
   if (plan->merge_tasks < 0 || plan->merge_items >= (1ll << 31)) return PA_ERR_UNSUPPORTED;
   return PA_OK;
 }
@@ -377,7 +431,7 @@ extern "C" pa_status pa_decode_plan(const pa_pool* pool, const int32_t* seq_lens
   pa_pool_desc d;
   if (!pool || (n_seq && !seq_lens_host)) return PA_ERR_INVALID;
   pa_pool_get_desc(pool, &d);
-  if (d.head_dim != kD || n_qtok < 1 || n_qtok > kMaxQTok) return PA_ERR_UNSUPPORTED;
+  if (d.head_dim != kD || n_qtok < 1 || n_qtok > (uint32_t)kMaxRowsQTok) return PA_ERR_UNSUPPORTED;
   if (n_seq == 0) return PA_ERR_INVALID;
   // Sub-batches of up to kInlineSeqs sequences: the largest grid, and the
   // tiles and partials summed over the sub-batches.
@@ -396,14 +450,14 @@ extern "C" pa_status pa_decode_plan(const pa_pool* pool, const int32_t* seq_lens
     // Pieces = CTA-range cuts plus segment cuts.
     long long base = 0;
     for (uint32_t s = 0; s < cn; ++s) {
-      const long long ntl = (lens[s] + geo.tile_keys - 1) / geo.tile_keys;
       for (int g = 0; g < geo.segs_per_seq; ++g) {
-        const long long a = base + g * ntl, e = a + ntl - 1;
+        const long long ntl = seg_tiles(geo, lens[s], n_qtok, g);
+        const long long a = base, e = a + ntl - 1;
+        base += ntl;
         const int c0p = (int)(((a + 1) * plan.ctas - 1) / plan.tiles);
         const int c1p = (int)(((e + 1) * plan.ctas - 1) / plan.tiles);
         pieces += (uint32_t)(c1p - c0p + 1);
       }
-      base += ntl * geo.segs_per_seq;
     }
   }
   if (n_ctas) *n_ctas = ctas;
@@ -438,8 +492,10 @@ static pa_status prepare_decode(const pa_pool* pool, const float* q, const void*
   if (cudaGetDevice(&device) != cudaSuccess) return PA_ERR_CUDA;
   st = make_plan(d, seq_lens_host, n_seq, n_qtok, table_stride, device, ki, plan);
   if (st != PA_OK) return st;
-  int sms = 0, occ = 0;
-  device_caps(device, d.k_type, d.v_type, (kGqa * (int)n_qtok + 7) / 8, *ki, &sms, &occ);
+  int sms = 0, occ = 0, slot = 0;
+  KernelInfo ki2;
+  pick_kernel(d.k_type, d.v_type, n_qtok, &ki2, &slot);
+  device_caps(device, d.k_type, d.v_type, slot, *ki, &sms, &occ);
   if (ws_bytes < workspace_bytes((long long)sms * occ, plan->n_seg, plan->geo.rows_per_seg)) return PA_ERR_INVALID;
 
   DecodeParams& p = *pp;
@@ -469,6 +525,7 @@ static pa_status prepare_decode(const pa_pool* pool, const float* q, const void*
   p.seg_heads = plan->geo.seg_heads;
   p.segs_per_seq = plan->geo.segs_per_seq;
   p.rows_per_seg = plan->geo.rows_per_seg;
+  p.n_row_tiles = plan->geo.n_row_tiles;
   p.scale_log2 = scale * kLog2e;
   for (uint32_t i = 0; i < n_seq; ++i) p.lens[i] = seq_lens_host[i];
   return PA_OK;
@@ -490,8 +547,9 @@ static pa_status launch_merge(const DecodeParams& p, const Plan& plan, const int
                               cudaStream_t cs) {
   static thread_local MergeParams<kCap> mp;  // up to 20 KB: kept off the stack
   mp.p = MergeCore{p.part_ml, p.part_o, p.out, p.lse, p.n_qtok, p.n_q_heads, p.seg_heads, p.segs_per_seq,
-                   p.rows_per_seg};
-  mp.n_tasks = list_merge_tasks(seq_lens_host, n_seq, plan.geo, plan.tiles, plan.ctas, mp.task, nullptr);
+                   p.rows_per_seg, p.n_row_tiles};
+  mp.n_tasks = list_merge_tasks(seq_lens_host, n_seq, (uint32_t)p.n_qtok, plan.geo, plan.tiles, plan.ctas, mp.task,
+                                nullptr);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)plan.merge_items);
   cfg.blockDim = dim3(kMergeThreads);

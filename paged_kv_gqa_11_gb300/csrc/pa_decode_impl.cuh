@@ -242,7 +242,8 @@ struct DecodeParams {
   int tile_keys;     // keys per tile: 16 (head groups) or 64 (single heads)
   int seg_heads;     // KV heads per segment: the head-group size, or 1
   int segs_per_seq;  // n_kv_heads / seg_heads
-  int rows_per_seg;  // query rows per segment: 6 * seg_heads * n_qtok
+  int rows_per_seg;  // query rows per segment: 6 * seg_heads * n_qtok, or a row tile
+  int n_row_tiles;   // row tiles per KV head (9 to 96 query tokens), else 0
   float scale_log2;  // scale * log2(e)
   // The host copy of the lengths (n_seq <= kInlineSeqs).  The tile walk, the
   // table reads and the masks use only these, so nothing the device copy

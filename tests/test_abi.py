@@ -158,7 +158,9 @@ def test_decode_rejects_unsupported_shapes_on_host(lib):
     args = dict(q=8192, k_pool=8192, v_pool=8192, block_table=8192, table_stride=8, seq_lens_dev=8192,
                 seq_lens_host=sl, n_seq=1, n_qtok=1, n_q_heads=24, scale=0.0625, out=8192, lse=None,
                 workspace=8192, ws_bytes=1 << 20, err=8192, stream=0, check=False)
-    assert pa.pa_decode(ok, **{**args, "n_qtok": 9}) == pa.PA_ERR_UNSUPPORTED
+    assert pa.pa_decode(ok, **{**args, "n_qtok": 97}) == pa.PA_ERR_UNSUPPORTED  # row tiles stop at 96
+    assert pa.pa_decode(ok, **{**args, "n_qtok": 0}) == pa.PA_ERR_UNSUPPORTED
+    assert pa.pa_decode(ok, **{**args, "n_qtok": 9}) == pa.PA_ERR_INVALID  # supported, but L = 5 < 9
     assert pa.pa_decode(ok, **{**args, "n_q_heads": 16}) == pa.PA_ERR_UNSUPPORTED
     assert pa.pa_decode(ok, **{**args, "q": None}) == pa.PA_ERR_INVALID
     assert pa.pa_decode(ok, **{**args, "q": 8196}) == pa.PA_ERR_INVALID   # not 16-byte aligned

@@ -366,6 +366,21 @@ def percall(length: int, n_qtok: int) -> Workload:
                          n_qtok, "shuffled")
 
 
+ROWS_CONTEXTS = (4096, 16384, 65536)
+ROWS_QTOK = (17, 65, 96)
+
+
+def rows_workload(context: int, n_qtok: int) -> Workload:
+    """The shape of the llama.cpp fork's row-tile table (PR #2, the commit on
+    ubatches of more than 8 tokens: chunked prefill against row tiles per
+    attention layer): one sequence of 4k / 16k / 64k cached tokens, of which
+    the last 17 / 65 / 96 are the query tokens.  The table gives no formats or
+    page size; the fork's production pair (Q8_0 K, Q4_0 V) in 256-row pages of
+    a shuffled pool is a reading, as for the per-call workload."""
+    return make_workload(f"rows-{context // 1024}k-{n_qtok}", 7, [context], 256, TYPE_Q8_0, TYPE_Q4_0, n_qtok,
+                         "shuffled")
+
+
 def _table_for(rng: np.random.Generator, lengths, ps: int, layout: str):
     """Block table of `lengths` for the 'interleaved' / 'shuffled' / 'identity'
     layouts of make_workload; returns (table, n_blocks)."""
