@@ -19,7 +19,7 @@
 #include <mutex>
 
 #include "pa.h"
-#include "pa_rows_impl.cuh"
+#include "pa_rows_tc.cuh"
 
 using namespace pa_dev;
 using namespace pa_split;
@@ -210,9 +210,9 @@ bool lookup_kernel(int kt, int vt, int nt, KernelInfo* out) {
   return false;
 }
 
-bool lookup_rows_kernel(int kt, int vt, KernelInfo* out) {
+bool lookup_rows_tc_kernel(int kt, int vt, KernelInfo* out) {
 #define PA_PAIR(k, v) \
-  if (kt == k && vt == v) return lookup_rows_kernel_##k##_##v(out);
+  if (kt == k && vt == v) return lookup_rows_tc_kernel_##k##_##v(out);
   PA_PAIR(1, 1) PA_PAIR(1, 2) PA_PAIR(1, 8)
   PA_PAIR(2, 1) PA_PAIR(2, 2) PA_PAIR(2, 8)
   PA_PAIR(8, 1) PA_PAIR(8, 2) PA_PAIR(8, 8)
@@ -231,7 +231,7 @@ bool pick_kernel(int kt, int vt, uint32_t n_qtok, KernelInfo* ki, int* slot) {
   }
   if (n_qtok > (uint32_t)kMaxQTok && n_qtok <= (uint32_t)kMaxRowsQTok) {
     *slot = kMaxNT;
-    return lookup_rows_kernel(kt, vt, ki);
+    return lookup_rows_tc_kernel(kt, vt, ki);
   }
   return false;
 }

@@ -4,8 +4,8 @@
 // lookup_kernel_<K>_<V>, returning the kernel for 1 to 6 n-tiles of 8 query
 // rows (6 rows per token: 1, 2, 3-4, 5, 6, 7-8 tokens); 6 to 8 tokens share
 // one kernel with two consumer groups.  Each unit also defines
-// lookup_rows_kernel_<K>_<V>, the row-tile kernel for 9 to 96 tokens.
-#include "pa_rows_impl.cuh"
+// lookup_rows_tc_kernel_<K>_<V>, the row-tile kernel for 9 to 96 tokens.
+#include "pa_rows_tc.cuh"
 
 #if !defined(PA_KT) || !defined(PA_VT)
 #error "compile with -DPA_KT=<pa_type> -DPA_VT=<pa_type>"
@@ -31,12 +31,12 @@ bool PA_LOOKUP_NAME(PA_KT, PA_VT)(int nt, KernelInfo* out) {
   }
 }
 
-#define PA_ROWS_LOOKUP_NAME_(k, v) lookup_rows_kernel_##k##_##v
-#define PA_ROWS_LOOKUP_NAME(k, v) PA_ROWS_LOOKUP_NAME_(k, v)
+#define PA_ROWS_TC_LOOKUP_NAME_(k, v) lookup_rows_tc_kernel_##k##_##v
+#define PA_ROWS_TC_LOOKUP_NAME(k, v) PA_ROWS_TC_LOOKUP_NAME_(k, v)
 
-// Row tiles for nine to 96 query tokens.
-bool PA_ROWS_LOOKUP_NAME(PA_KT, PA_VT)(KernelInfo* out) {
-  *out = rows_kernel_info<PA_KT, PA_VT>();
+// Row tiles (nine to 96 query tokens) on the fifth-generation tensor core.
+bool PA_ROWS_TC_LOOKUP_NAME(PA_KT, PA_VT)(KernelInfo* out) {
+  *out = rows_tc_kernel_info<PA_KT, PA_VT>();
   return true;
 }
 
