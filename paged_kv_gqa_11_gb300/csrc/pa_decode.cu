@@ -220,16 +220,23 @@ bool lookup_rows_tc_kernel(int kt, int vt, KernelInfo* out) {
   return false;
 }
 
-// The split kernel for n_qtok query tokens: the decode kernels up to eight
-// tokens (by n-tiles of 8 query rows), the row-tile kernel from nine to 96.
-// *slot: its index in the occupancy cache.
+// Query tokens from which the row-tile kernel takes over from the decode
+// kernels.
+#ifndef PA_ROWS_FROM
+#define PA_ROWS_FROM 9
+#endif
+constexpr uint32_t kRowsFromQTok = PA_ROWS_FROM;
+
+// The split kernel for n_qtok query tokens: the decode kernels below
+// kRowsFromQTok tokens (by n-tiles of 8 query rows), the row-tile kernel from
+// there to 96.  *slot: its index in the occupancy cache.
 bool pick_kernel(int kt, int vt, uint32_t n_qtok, KernelInfo* ki, int* slot) {
-  if (n_qtok >= 1 && n_qtok <= (uint32_t)kMaxQTok) {
+  if (n_qtok >= 1 && n_qtok < kRowsFromQTok && n_qtok <= (uint32_t)kMaxQTok) {
     const int nt = (kGqa * (int)n_qtok + 7) / 8;
     *slot = nt - 1;
     return lookup_kernel(kt, vt, nt, ki);
   }
-  if (n_qtok > (uint32_t)kMaxQTok && n_qtok <= (uint32_t)kMaxRowsQTok) {
+  if (n_qtok >= kRowsFromQTok && n_qtok <= (uint32_t)kMaxRowsQTok) {
     *slot = kMaxNT;
     return lookup_rows_tc_kernel(kt, vt, ki);
   }
@@ -283,7 +290,7 @@ pa_status check_shape(const pa_pool* pool, uint32_t n_qtok, uint32_t n_q_heads, 
 // (16 keys of up to four KV heads; the group is the largest of 4, 3, 2, 1 that
 // divides the KV head count), two to eight tokens per-head tiles of 64 keys,
 // and nine to 96 tokens row tiles (segments of 128 query rows of one KV head,
-// 64-key tiles).
+// 32-key tiles).
 struct Geometry {
   int tile_keys, seg_heads, segs_per_seq, rows_per_seg;
   int n_row_tiles;  // row tiles per KV head, or 0
@@ -292,8 +299,8 @@ struct Geometry {
 Geometry geometry(const pa_pool_desc& d, uint32_t n_qtok) {
   Geometry g;
   g.n_row_tiles = 0;
-  if (n_qtok > (uint32_t)kMaxQTok) {
-    g.tile_keys = kTile;
+  if (n_qtok >= kRowsFromQTok) {
+    g.tile_keys = kRowKeys;
     g.seg_heads = 1;
     g.n_row_tiles = (kGqa * (int)n_qtok + kRowTile - 1) / kRowTile;
     g.segs_per_seq = (int)d.n_kv_heads * g.n_row_tiles;
@@ -316,7 +323,7 @@ Geometry geometry(const pa_pool_desc& d, uint32_t n_qtok) {
 }
 
 // Tiles of segment gi of a sequence of length L (the device side's
-// tiles_of / row_seg_tiles): a row tile takes the 64-key tiles its last row
+// tiles_of / row_seg_tiles): a row tile takes the key tiles its last row
 // sees.
 long long seg_tiles(const Geometry& geo, long long L, uint32_t n_qtok, int gi) {
   if (geo.n_row_tiles == 0) return (L + geo.tile_keys - 1) / geo.tile_keys;

@@ -6,7 +6,7 @@
 // than a chunked prefill up to 96 query tokens (llama.cpp fork PR #2, the
 // commit on KV-streaming ubatches of more than 8 tokens).  With 6 * n_qtok
 // query rows per KV head the rows are the MMA's M dimension: a segment is
-// (sequence, KV head, row tile of 128 rows), and its tiles are the 64-key tiles
+// (sequence, KV head, row tile of 128 rows), and its tiles are the 32-key tiles
 // its last row can see, so early row tiles of a long verify batch stop short of
 // the newest keys.  Segments are cut into pieces by the same stream-K planner as
 // the decode kernels and merged by the same LSE merge.
@@ -17,19 +17,26 @@
 namespace pa_split {
 
 constexpr int kRowTile = 128;                  // query rows per row tile
-constexpr int kRowWarps = 8;                   // warps of a row-tile CTA
-constexpr int kRowThreads = kRowWarps * 32;
+constexpr int kRowKeys = 32;                   // keys per row-tile key tile (two row groups)
 constexpr int kMaxRowsQTok = 96;               // query tokens the row tiles take
-constexpr uint32_t kRowBar = 1;                // named barrier of the consumer warps
+
+// A stage of one key tile: its two K row groups, then its two V row groups.
+template <int KT, int VT>
+struct RowStageGeo {
+  static constexpr int kKGroup = pa_layout::group_bytes<KT>();
+  static constexpr int kVGroup = pa_layout::group_bytes<VT>();
+  static constexpr int kKBytes = 2 * kKGroup;
+  static constexpr int kBytes = 2 * (kKGroup + kVGroup);
+};
 
 // ------------------------------------------------------------------ the walk
 
 // Tiles of segment gi (KV head gi / n_row_tiles, row tile gi % n_row_tiles) of
-// a sequence of length L: the 64-key tiles that the tile's last row sees.
+// a sequence of length L: the 32-key tiles that the tile's last row sees.
 __device__ __forceinline__ int row_seg_tiles(const DecodeParams& p, int L, int gi) {
   const int rt = gi % p.n_row_tiles;
   const int t_last = min(p.n_qtok - 1, (kRowTile * (rt + 1) - 1) / kGqa);
-  return (L - p.n_qtok + t_last + 1 + kTile - 1) / kTile;
+  return (L - p.n_qtok + t_last + 1 + kRowKeys - 1) / kRowKeys;
 }
 
 struct RowPos {
@@ -70,32 +77,32 @@ __device__ __forceinline__ void row_next(const DecodeParams& p, RowPos& t) {
 
 // ------------------------------------------------------------------ stage copies
 
-// Table entry of row group `lane` (0..3) of tile t, or -1 for lanes past the
-// tile's row groups.
+// Table entry of row group `lane` (0..1) of key tile t, or -1 for lanes past
+// the tile's row groups.
 __device__ __forceinline__ int row_entry(const DecodeParams& p, const RowPos& t, int lane) {
-  const int k0 = t.j * kTile, n = min(kTile, t.L - k0);
-  if (lane >= 4 || lane * kGroup >= n || t.s >= p.n_seq) return -1;
+  const int k0 = t.j * kRowKeys, n = min(kRowKeys, t.L - k0);
+  if (lane >= 2 || lane * kGroup >= n || t.s >= p.n_seq) return -1;
   return __ldg(p.table + (long long)t.s * p.table_stride + (k0 + lane * kGroup) / p.page_size);
 }
 
-// Warp 0 fills one stage with tile t (four row groups of one KV head, K then
-// V); tb: this lane's table entry (row_entry).  Groups past the sequence's
-// last key are not copied; a group whose entry is outside the pool is
-// zero-filled and reported.  The whole warp calls this.
+// Fill one stage with key tile t (two row groups of one KV head, K then V);
+// tb: this lane's table entry (row_entry).  Groups past the sequence's last
+// key are not copied; a group whose entry is outside the pool is zero-filled
+// and reported.  The whole warp calls this.
 template <int KT, int VT>
 __device__ __forceinline__ void issue_stage(const DecodeParams& p, const RowPos& t, int tb, uint32_t sk, uint32_t fb,
                                             uint64_t policy, int lane) {
-  using G = StageGeo<KT, VT>;
+  using G = RowStageGeo<KT, VT>;
   constexpr int RK = Fmt<KT>::kRow, RV = Fmt<VT>::kRow;
   const int head = t.gi / p.n_row_tiles;
-  const int k0 = t.j * kTile, n = min(kTile, t.L - k0), ng = (n + kGroup - 1) / kGroup;
+  const int k0 = t.j * kRowKeys, n = min(kRowKeys, t.L - k0), ng = (n + kGroup - 1) / kGroup;
   const uint32_t sv = sk + G::kKBytes;
   const bool mine = lane < ng;
   const bool ok = !mine || (tb >= 0 && tb < p.n_blocks);
   const unsigned bad = __ballot_sync(0xffffffffu, !ok);
   if (bad) {
     if (lane == 0) record_error(p.err, PA_ERR_BOUNDS);
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < 2; ++q) {
       if (!((bad >> q) & 1)) continue;
       for (int i = lane; i < G::kKGroup / 16; i += 32) sts128_zero(sk + q * G::kKGroup + 16 * i);
       for (int i = lane; i < G::kVGroup / 16; i += 32) sts128_zero(sv + q * G::kVGroup + 16 * i);

@@ -10,26 +10,35 @@
 // dense contraction, so it runs on tcgen05:
 //
 //   segment  = (sequence, KV head, row tile of 128 query rows); its tiles are
-//              the 64-key tiles the row tile's last row sees;
-//   S        = Q K^T    tcgen05.mma M = 128 rows, N = 64 keys, K = 256 dims,
-//                       fp32 in tensor memory (64 columns);
-//   softmax  four warps, one thread per query row: the row's 64 logits come
-//            from tensor memory into registers (no shuffles), causal mask,
-//            lazy online maximum (raised only past 2^8; then that row of O is
-//            rescaled in tensor memory), P as binary16 into shared memory;
-//   O       += P V     tcgen05.mma M = 128 rows, N = 256 dims, K = 64 keys,
+//              the 32-key tiles the row tile's last row sees;
+//   S        = Q K^T    tcgen05.mma M = 128 rows, N = 32 keys, K = 256 dims,
+//                       fp32 in tensor memory (two 32-column buffers);
+//   softmax  one thread per query row: the row's logits come from tensor
+//            memory into registers (no shuffles), causal mask, lazy online
+//            maximum (raised only past 2^8; then that row of O is rescaled in
+//            tensor memory), P as binary16 into shared memory;
+//   O       += P V     tcgen05.mma M = 128 rows, N = 256 dims, K = 32 keys,
 //                       fp32 in tensor memory (256 columns).
+//
+// The CTA's warps specialise and run as a pipeline over its key tiles, each
+// hand-off an mbarrier:
+//   warps 0-3  softmax and output, one query row per thread (tensor-memory
+//              lane quarters 0-3);
+//   warps 4-7  dequantisation: eight keys each per tile, K and V into
+//              double-buffered binary16 tiles (and Q at a segment start);
+//   warp 8     issues the MMAs (one thread): S of tile j + 1 goes to the tensor
+//              core before O += P V of tile j, so S is computed while the
+//              softmax of the previous tile runs;
+//   warp 9     streams raw K/V row groups into a ring of stages (bulk copies).
 //
 // Operands sit in shared memory in the MMA's canonical no-swizzle K-major
 // layout (core matrices of 8 rows x 16 bytes): Q [rows][dims], K [keys][dims],
-// V^T [dims][keys] and P [rows][keys].  Raw K/V row groups stream into a ring
-// of stages with bulk copies (one lane of warp 0 refills a stage once every
-// warp has dequantised it); each warp dequantises eight keys per tile: ldmatrix
-// reads the raw quants (thread 4g+t gets four bytes of key g), the values are
-// converted in registers and stmatrix writes them as core matrices (.trans
-// for V), without bank conflicts.  That fixes a per-format order of the head
-// dims inside each 32-dim window (dim_of below); Q is staged in K's order and O
-// is written back through V's.
+// V^T [dims][keys] and P [rows][keys].  Dequantisation reads the raw quants
+// with ldmatrix (thread 4g+t gets four bytes of key g), converts them in
+// registers and writes core matrices with stmatrix (.trans for V), without
+// bank conflicts.  That fixes a per-format order of the head dims inside each
+// 32-dim window (dim_of below); Q is staged in K's order and O is written back
+// through V's.
 //
 // Precision: Q, P and V (q * d rounded once) are binary16.  Quantised K is
 // kept to about 2^-22: it is split as K = K_hi + K_lo, K_hi = q * d rounded to
@@ -42,28 +51,37 @@
 
 namespace pa_split {
 
-constexpr uint32_t kTcTmemCols = 512;     // S at column 0 (64), O at column 256 (256)
+constexpr uint32_t kTcTmemCols = 512;  // S buffers at columns 0 and 32, O at column 256
 constexpr uint32_t kTcOCol = 256;
-constexpr uint32_t kTcIdescS = idesc_f16_f32(kRowTile, kTile);  // 128 x 64
-constexpr uint32_t kTcIdescO = idesc_f16_f32(kRowTile, kD);     // 128 x 256
+constexpr uint32_t kTcIdescS = idesc_f16_f32(kRowTile, kRowKeys);  // 128 x 32
+constexpr uint32_t kTcIdescO = idesc_f16_f32(kRowTile, kD);        // 128 x 256
+constexpr int kTcSmWarps = 4, kTcDqWarp0 = 4, kTcMmaWarp = 8, kTcCopyWarp = 9;
+constexpr int kRowThreads = 10 * 32;
 
 template <int KT, int VT>
 struct TcSmem {
-  static constexpr bool kKSplit = KT != PA_F16;                  // K_hi and K_lo
-  static constexpr int kStageBytes = StageGeo<KT, VT>::kBytes;   // 64 keys raw: 4 K groups then 4 V groups
-  static constexpr int kQ = 0;                                   // Q   [128][256] binary16: 64 KB
-  static constexpr int kKh = kQ + kRowTile * kD * 2;             // K   [64][256]  (K_hi): 32 KB
-  static constexpr int kKl = kKh + kTile * kD * 2;               // K_lo, then P (once S is done): 32 KB
-  static constexpr int kP = kKSplit ? kKl : kKl;                 // P   [128][64]: 16 KB
-  static constexpr int kVt = kKl + (kKSplit ? kTile * kD * 2 : kRowTile * kTile * 2);  // V^T [256][64]: 32 KB
-  static constexpr int kRing = kVt + kD * kTile * 2;
-  static constexpr int kFit = (232448 - 1024 - kAlign - kRing - 256) / kStageBytes;
-  static constexpr int kStages = kFit > 3 ? 3 : kFit;
-  static_assert(kStages >= 1, "tcgen05 row-tile stage does not fit");
-  static constexpr int kBar = kRing + kStages * kStageBytes;    // full[kStages], s_done, pv_done, drain
-  static constexpr int kMisc = kBar + (kStages + 3) * 8;        // abort, start[3], tmem base
+  static constexpr bool kKSplit = KT != PA_F16;  // K_hi and K_lo
+  static constexpr int kStageBytes = RowStageGeo<KT, VT>::kBytes;
+  static constexpr int kKBytes = kRowKeys * kD * 2;  // one K tile [32][256]: 16 KB
+  static constexpr int kVBytes = kD * kRowKeys * 2;  // one V^T tile [256][32]: 16 KB
+  static constexpr int kPBytes = kRowTile * kRowKeys * 2;  // one P tile [128][32]: 8 KB
+  static constexpr int kBuf = kKBytes * (kKSplit ? 2 : 1) + kVBytes + kPBytes;  // one buffer: K_hi [K_lo] V^T P
+  static constexpr int kQ = 0;                       // Q [128][256]: 64 KB
+  static constexpr int kBuf0 = kQ + kRowTile * kD * 2;
+  static constexpr int kKh = 0, kKl = kKBytes, kVt = kKBytes * (kKSplit ? 2 : 1), kP = kVt + kVBytes;
+  static constexpr int kRing = kBuf0 + 2 * kBuf;
+  static constexpr int kFit = (232448 - 1024 - kRing - 512) / kStageBytes;
+  static constexpr int kStages = kFit > 4 ? 4 : kFit;
+  static_assert(kStages >= 2, "row-tile stage ring does not fit");
+  static_assert(kRing % 1024 == 0, "tile alignment");
+  // mbarriers: raw full / empty [kStages], kv full / empty [2], s full / empty
+  // [2], p full [2], drain
+  static constexpr int kBar = kRing + kStages * kStageBytes;
+  static constexpr int kNBar = 2 * kStages + 8 + 1;
+  static constexpr int kMisc = kBar + kNBar * 8;  // abort, start[3], tmem base
   static constexpr int kTotal = kMisc + 32;
-  static constexpr int kLaunch = kTotal + kAlign;
+  static constexpr int kLaunch = kTotal + 1024;  // the base is aligned to 1024 inside
+  static_assert(kTotal - kRing - kStages * kStageBytes <= 512, "barrier area");
 };
 
 // Canonical K-major offsets (bytes): operand with `kslots` 8-element slots
@@ -92,7 +110,7 @@ template <bool kRoleV>
 __device__ __forceinline__ void tc_store4(uint32_t dst, int w, int lane, int s0, uint32_t r0, uint32_t r1, uint32_t r2,
                                           uint32_t r3) {
   const int mj = lane >> 3, mr = lane & 7;
-  if (kRoleV) stsm_x4_trans(dst + canon_off(8 * (s0 + mj) + mr, w, kTile / 8), r0, r1, r2, r3);
+  if (kRoleV) stsm_x4_trans(dst + canon_off(8 * (s0 + mj) + mr, w, kRowKeys / 8), r0, r1, r2, r3);
   else stsm_x4(dst + canon_off(8 * w + mr, s0 + mj, kD / 8), r0, r1, r2, r3);
 }
 
@@ -103,8 +121,8 @@ __device__ __forceinline__ uint32_t tc_lo(uint32_t v, uint32_t d2, uint32_t hi) 
   return hfma2(v, d2, hi ^ 0x80008000u);
 }
 
-// Warp w's eight keys (8w .. 8w+7) of a raw 64-key stage region of format T
-// (four row groups), as binary16 core matrices: V values q * d into the V^T
+// Eight keys (8w .. 8w+7) of a raw 32-key stage region of format T (two row
+// groups), as binary16 core matrices: V values q * d into the V^T
 // tile (kRoleV), K exact for F16 or as K_hi / K_lo tiles for Q8_0 and Q4_0.
 // Keys at or past n_keys are written as zeros.
 template <int T, bool kRoleV>
@@ -184,7 +202,7 @@ template <int KT>
 __device__ __forceinline__ void tc_stage_q(const DecodeParams& p, int s, int head, int rt, uint32_t qsm, int tid) {
   const int R = kGqa * p.n_qtok;
 #pragma unroll 1
-  for (int task = tid; task < kRowTile * (kD / 32); task += kRowTile * 2) {
+  for (int task = tid; task < kRowTile * (kD / 32); task += 4 * 32) {  // tid: 0 .. 127
     const int row = task & (kRowTile - 1), win = task >> 7, rg = kRowTile * rt + row;
     float v[32];
     if (rg < R) {
@@ -215,22 +233,44 @@ __device__ __forceinline__ void tc_stage_q(const DecodeParams& p, int s, int hea
 
 // ------------------------------------------------------------------ the kernel
 
+// A tile's place in the CTA's walk, as every role sees it.
+struct TcTile {
+  RowPos pos;    // segment and tile
+  bool first;    // the first tile of a piece (a new segment, or the CTA's first)
+  bool last;     // the last tile of a piece
+};
+
+__device__ __forceinline__ TcTile tc_tile(const RowPos& pos, long long x, long long a, long long b) {
+  return TcTile{pos, x == a || pos.j == 0, x + 1 == b || pos.j + 1 == pos.nt};
+}
+
 template <int KT, int VT>
 __global__ void __launch_bounds__(kRowThreads, 1) pa_rows_tc_kernel(const __grid_constant__ DecodeParams p) {
   using SM = TcSmem<KT, VT>;
-  using G = StageGeo<KT, VT>;
+  using G = RowStageGeo<KT, VT>;
   constexpr int kStages = SM::kStages;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
-  uint8_t* smem = smem_raw + ((kAlign - (raw & (kAlign - 1))) & (kAlign - 1));
+  uint8_t* smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
   const uint32_t base = smem_u32(smem);
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
-  const uint32_t bar_full = base + SM::kBar, bar_s = bar_full + 8 * kStages, bar_pv = bar_s + 8,
-                 bar_drain = bar_pv + 8;
+  const uint32_t bars = base + SM::kBar;
+  const uint32_t raw_full = bars, raw_empty = bars + 8 * kStages;
+  // Hand-offs (b = j & 1 is tile j's buffer, u = j >> 1 its use of it; every
+  // wait below is on a phase that cannot be two ahead of the waiter):
+  //   raw_full / raw_empty  copy warp <-> dequantisation, per ring stage
+  //   kv_full   dequantisation -> MMA: K and V^T of tile j in buffer b
+  //   kv_empty  MMA commit after O += P V of tile j: buffer b free again; also
+  //             "O holds tiles .. j" for the softmax warps
+  //   s_full    MMA commit after S(j); s_empty: softmax has S(j) in registers
+  //   p_full    softmax -> MMA: P of tile j in buffer b
+  const uint32_t kv_full = bars + 16 * kStages, kv_empty = kv_full + 16, s_full = kv_full + 32,
+                 s_empty = kv_full + 48, p_full = kv_full + 64, drain = kv_full + 80;
   volatile int* abort = reinterpret_cast<volatile int*>(smem + SM::kMisc);
   int* start = reinterpret_cast<int*>(smem + SM::kMisc + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM::kMisc + 16);
   const uint32_t ring = base + SM::kRing;
+  auto buf = [&](int bb) { return base + SM::kBuf0 + bb * SM::kBuf; };
 
   const long long T = p.total_tiles;
   const int Gn = p.n_ctas;
@@ -239,10 +279,18 @@ __global__ void __launch_bounds__(kRowThreads, 1) pa_rows_tc_kernel(const __grid
   if (tid == 0) {
     asm volatile("griddepcontrol.launch_dependents;");
     *abort = 0;
-    for (int i = 0; i < kStages; ++i) mbar_init(bar_full + 8 * i, 1);
-    mbar_init(bar_s, 1);
-    mbar_init(bar_pv, 1);
-    mbar_init(bar_drain, 1);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(raw_full + 8 * i, 1);
+      mbar_init(raw_empty + 8 * i, 4);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(kv_full + 8 * i, 4);
+      mbar_init(kv_empty + 8 * i, 1);
+      mbar_init(s_full + 8 * i, 1);
+      mbar_init(s_empty + 8 * i, kTcSmWarps);
+      mbar_init(p_full + 8 * i, kTcSmWarps);
+    }
+    mbar_init(drain, 1);
     fence_mbar_init();
     const RowPos r = row_locate(p, a);
     start[0] = r.s;
@@ -258,202 +306,237 @@ __global__ void __launch_bounds__(kRowThreads, 1) pa_rows_tc_kernel(const __grid
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const bool any = start[0] < p.n_seq;  // the planner gives every CTA a tile
-  RowPos pos;
-  pos.s = start[0];
-  pos.gi = start[1];
-  pos.j = start[2];
-  pos.L = any ? p.lens[pos.s] : 0;
-  pos.nt = any ? row_seg_tiles(p, pos.L, pos.gi) : 0;
-
-  // Raw stage copies (warp 0): tiles a .. a + kStages - 1 now, then tile
-  // x + kStages once every warp has dequantised tile x from its slot.
-  const uint64_t policy = l2_evict_first_policy();
-  RowPos ipos = pos;
-  long long issued = a;
-  int ientry = -1;
-  if (w == 0 && any) {
-    ientry = row_entry(p, ipos, lane);
-    for (; issued < b && issued < a + kStages; ++issued) {
-      const int slot = (int)(issued - a);
-      issue_stage<KT, VT>(p, ipos, ientry, ring + slot * G::kBytes, bar_full + 8 * slot, policy, lane);
-      row_next(p, ipos);
-      ientry = row_entry(p, ipos, lane);
-    }
-  }
-
+  RowPos pos0;
+  pos0.s = start[0];
+  pos0.gi = start[1];
+  pos0.j = start[2];
+  pos0.L = any ? p.lens[pos0.s] : 0;
+  pos0.nt = any ? row_seg_tiles(p, pos0.L, pos0.gi) : 0;
   const int R = kGqa * p.n_qtok;
-  const float scale_log2 = p.scale_log2;
-  const uint32_t t_lane = (uint32_t)(32 * (w & 3)) << 16;  // this warp's tensor-memory lanes
-  const uint32_t tS = tmem + t_lane, tO = tmem + kTcOCol + t_lane;
-  int st = 0;
-  uint32_t ph = 0, nt_done = 0;  // full-barrier ring position; tiles done (S / PV barrier parity)
-  long long x = a;
-  while (any && x < b) {
-    const int s = pos.s, gi = pos.gi, L = pos.L, ntl = pos.nt;
-    const int head = gi / p.n_row_tiles, rt = gi % p.n_row_tiles;
-    const int l_dev = device_len(p, s);
-    const int jb = pos.j, je = (int)((long long)ntl < jb + (b - x) ? (long long)ntl : jb + (b - x));
-    const int seg = s * p.segs_per_seq + gi;
-    const bool whole = (jb == 0 && je == ntl);
-    tc_stage_q<KT>(p, s, head, rt, base + SM::kQ, tid);
-    fence_proxy_async_smem();
-    // softmax threads: warps 0..3, one query row each
-    const int row = 32 * w + lane, rg = kRowTile * rt + row;
-    const bool smx = w < 4 && kRowTile * rt + 32 * w < R;  // the warp holds a real row
-    const int vis = rg < R ? L - p.n_qtok + rg / kGqa : -1;
-    float m = -INFINITY, l = 0.f;
 
-    for (int jt = jb; jt < je; ++jt) {
-      const int k0 = jt * kTile, n_keys = min(kTile, L - k0);
-      const uint32_t sk = ring + st * G::kBytes, sv = sk + G::kKBytes;
-      mbar_wait(bar_full + 8 * st, ph, p.err, abort);
-      tc_dequant_warp<KT, false>(sk, base + SM::kKh, base + SM::kKl, w, lane, n_keys);
-      tc_dequant_warp<VT, true>(sv, base + SM::kVt, 0u, w, lane, n_keys);
-      fence_proxy_async_smem();
-      tc_fence_before();
-      named_bar_sync(kRowBar, kRowThreads);  // Q, K and V^T tiles ready; the stage is free
-      if (w == 0 && issued < b) {
-        issue_stage<KT, VT>(p, ipos, ientry, ring + st * G::kBytes, bar_full + 8 * st, policy, lane);
-        ++issued;
-        row_next(p, ipos);
-        ientry = row_entry(p, ipos, lane);
+  if (any && w == kTcCopyWarp) {
+    // ---- raw K/V stages
+    const uint64_t policy = l2_evict_first_policy();
+    RowPos pos = pos0;
+    for (long long x = a; x < b; ++x) {
+      if (__any_sync(0xffffffffu, *abort != 0)) break;
+      const int j = (int)(x - a), slot = j % kStages, use = j / kStages;
+      if (use > 0) mbar_wait(raw_empty + 8 * slot, (use - 1) & 1, p.err, abort);
+      const int tb = row_entry(p, pos, lane);
+      issue_stage<KT, VT>(p, pos, tb, ring + slot * G::kBytes, raw_full + 8 * slot, policy, lane);
+      row_next(p, pos);
+    }
+  } else if (any && w >= kTcDqWarp0 && w < kTcDqWarp0 + 4) {
+    // ---- dequantisation (and Q at every segment start)
+    const int dw = w - kTcDqWarp0, dtid = tid - 32 * kTcDqWarp0;
+    RowPos pos = pos0;
+    for (long long x = a; x < b; ++x) {
+      const TcTile tt = tc_tile(pos, x, a, b);
+      const int j = (int)(x - a), bb = j & 1, use = j >> 1;
+      if (tt.first) {
+        // the previous piece's S is done with Q before it is overwritten
+        if (j > 0) mbar_wait(s_full + 8 * ((j - 1) & 1), ((j - 1) >> 1) & 1, p.err, abort);
+        tc_stage_q<KT>(p, pos.s, pos.gi / p.n_row_tiles, pos.gi % p.n_row_tiles, base + SM::kQ, dtid);
       }
-      if (tid == 4 * 32) {  // S = Q K^T (+ Q K_lo^T)
+      const int slot = j % kStages;
+      mbar_wait(raw_full + 8 * slot, (j / kStages) & 1, p.err, abort);
+      if (use > 0) mbar_wait(kv_empty + 8 * bb, (use - 1) & 1, p.err, abort);  // tile j - 2 is done with it
+      __syncwarp();
+      const int n_keys = min(kRowKeys, pos.L - pos.j * kRowKeys);
+      const uint32_t sk = ring + slot * G::kBytes, bk = buf(bb);
+      tc_dequant_warp<KT, false>(sk, bk + SM::kKh, bk + SM::kKl, dw, lane, n_keys);
+      tc_dequant_warp<VT, true>(sk + G::kKBytes, bk + SM::kVt, 0u, dw, lane, n_keys);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(raw_empty + 8 * slot);
+        mbar_arrive(kv_full + 8 * bb);
+      }
+      row_next(p, pos);
+    }
+  } else if (any && w == kTcMmaWarp) {
+    // ---- MMA issue (one thread): S(j), then O += P V of tile j - 1
+    if (lane == 0) {
+      auto pv = [&](int jj, bool first) {  // O (+)= P V of tile jj
+        const int pb = jj & 1;
+        mbar_wait(p_full + 8 * pb, (jj >> 1) & 1, p.err, abort);
         tc_fence_after();
+        const uint32_t pk = buf(pb);
+#pragma unroll
+        for (int kk = 0; kk < kRowKeys / 16; ++kk)
+          tc_mma_f16(tmem + kTcOCol, smem_desc(pk + SM::kP + 256 * kk, 128, 512),
+                     smem_desc(pk + SM::kVt + 256 * kk, 128, 512), kTcIdescO, (first && kk == 0) ? 0u : 1u);
+        tc_commit(kv_empty + 8 * pb);
+      };
+      RowPos pos = pos0;
+      bool prev_first = false;
+      for (long long x = a; x < b; ++x) {
+        const int j = (int)(x - a), bb = j & 1, use = j >> 1;
+        const bool first = tc_tile(pos, x, a, b).first;
+        mbar_wait(kv_full + 8 * bb, use & 1, p.err, abort);
+        if (use > 0) mbar_wait(s_empty + 8 * bb, (use - 1) & 1, p.err, abort);
+        tc_fence_after();
+        const uint32_t bk = buf(bb), dS = tmem + kRowKeys * bb;
 #pragma unroll
         for (int ks = 0; ks < kD / 16; ++ks)
-          tc_mma_f16(tmem, smem_desc(base + SM::kQ + 256 * ks, 128, 4096),
-                     smem_desc(base + SM::kKh + 256 * ks, 128, 4096), kTcIdescS, ks > 0);
+          tc_mma_f16(dS, smem_desc(base + SM::kQ + 256 * ks, 128, 4096), smem_desc(bk + SM::kKh + 256 * ks, 128, 4096),
+                     kTcIdescS, ks > 0);
         if (SM::kKSplit) {
 #pragma unroll
           for (int ks = 0; ks < kD / 16; ++ks)
-            tc_mma_f16(tmem, smem_desc(base + SM::kQ + 256 * ks, 128, 4096),
-                       smem_desc(base + SM::kKl + 256 * ks, 128, 4096), kTcIdescS, 1);
+            tc_mma_f16(dS, smem_desc(base + SM::kQ + 256 * ks, 128, 4096),
+                       smem_desc(bk + SM::kKl + 256 * ks, 128, 4096), kTcIdescS, 1);
         }
-        tc_commit(bar_s);
+        tc_commit(s_full + 8 * bb);
+        if (j > 0) pv(j - 1, prev_first);
+        prev_first = first;
+        row_next(p, pos);
       }
-      if (smx) {
-        mbar_wait(bar_s, nt_done & 1, p.err, abort);
-        __syncwarp();  // tensor-memory loads are warp-wide
+      if (b > a) pv((int)(b - a) - 1, prev_first);
+    }
+    __syncwarp();
+  } else if (any && w < kTcSmWarps) {
+    // ---- softmax and output: one query row per thread
+    const int row = 32 * w + lane;
+    const uint32_t t_lane = (uint32_t)(32 * w) << 16;
+    const uint32_t tO = tmem + kTcOCol + t_lane;
+    const float scale_log2 = p.scale_log2;
+    RowPos pos = pos0;
+    float m = -INFINITY, l = 0.f;
+    int vis = -1, piece_j0 = 0;
+    bool piece_whole = false;
+    for (long long x = a; x < b; ++x) {
+      const TcTile tt = tc_tile(pos, x, a, b);
+      const int j = (int)(x - a), bb = j & 1, use = j >> 1;
+      const int rt = pos.gi % p.n_row_tiles, rg = kRowTile * rt + row;
+      const bool smx = kRowTile * rt + 32 * w < R;  // the warp holds a real row
+      if (tt.first) {
+        m = -INFINITY;
+        l = 0.f;
+        vis = rg < R ? pos.L - p.n_qtok + rg / kGqa : -1;
+        piece_j0 = j;
+        piece_whole = pos.j == 0;
+      }
+      const int k0 = pos.j * kRowKeys;
+      // S of tile j: into registers, then the buffer is free for S(j + 2)
+      mbar_wait(s_full + 8 * bb, use & 1, p.err, abort);
+      __syncwarp();
+      tc_fence_after();
+      uint32_t sv[32];
+      tmem_ld32(tmem + t_lane + kRowKeys * bb, sv);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_empty + 8 * bb);
+      float tmax = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kRowKeys; ++c) {
+        const float v = (k0 + c <= vis) ? __uint_as_float(sv[c]) * scale_log2 : -INFINITY;
+        sv[c] = __float_as_uint(v);
+        tmax = fmaxf(tmax, v);
+      }
+      // Lazy maximum: raised (rarely, after a row's first tile) past 2^8.  The
+      // rows of O that hold weight are rescaled in tensor memory once the
+      // previous O += P V is done; the tensor-memory loads and stores are
+      // warp-wide, so the whole warp runs them when any of its rows rises.
+      const bool raise = tmax > m + kLazy;
+      const float al = raise ? ((m == -INFINITY) ? 1.f : ex2(m - tmax)) : 1.f;
+      if (smx && __any_sync(0xffffffffu, raise) && j > piece_j0) {
+        mbar_wait(kv_empty + 8 * ((j - 1) & 1), ((j - 1) >> 1) & 1, p.err, abort);  // O holds tile j - 1
+        __syncwarp();
         tc_fence_after();
-        uint32_t sv32[2][32];
-        tmem_ld32(tS, sv32[0]);
-        tmem_ld32(tS + 32, sv32[1]);
-        tmem_ld_wait();
-        float tmax = -INFINITY;
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const float v = (k0 + 32 * h + c <= vis) ? __uint_as_float(sv32[h][c]) * scale_log2 : -INFINITY;
-            sv32[h][c] = __float_as_uint(v);
-            tmax = fmaxf(tmax, v);
-          }
-        // Lazy maximum: raised (rarely, after a row's first tile) past 2^8.
-        // The rows of O that hold weight are rescaled in tensor memory; the
-        // tensor-memory loads and stores are warp-wide (.sync.aligned), so the
-        // whole warp runs them when any of its rows rises.
-        const bool raise = tmax > m + kLazy;
-        const float al = raise ? ((m == -INFINITY) ? 1.f : ex2(m - tmax)) : 1.f;
-        if (__any_sync(0xffffffffu, raise) && jt > jb) {
 #pragma unroll 1
-          for (int c = 0; c < kD; c += 32) {
-            uint32_t ov[32];
-            tmem_ld32(tO + c, ov);
-            tmem_ld_wait();
+        for (int c = 0; c < kD; c += 32) {
+          uint32_t ov[32];
+          tmem_ld32(tO + c, ov);
+          tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * al);
-            tmem_st32(tO + c, ov);
+          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * al);
+          tmem_st32(tO + c, ov);
+        }
+        tmem_st_wait();
+      }
+      if (raise) {
+        l *= al;
+        m = tmax;
+      }
+      // P of tile j into buffer bb, once tile j - 2's O += P V is done with it
+      if (use > 0) mbar_wait(kv_empty + 8 * bb, (use - 1) & 1, p.err, abort);
+      const float bm = (m == -INFINITY) ? 0.f : m;
+      const uint32_t pk = buf(bb) + SM::kP;
+#pragma unroll
+      for (int kc = 0; kc < kRowKeys / 8; ++kc) {
+        uint32_t ph4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int c = 8 * kc + 2 * e;
+          ph4[e] = pack_half2(ex2(__uint_as_float(sv[c]) - bm), ex2(__uint_as_float(sv[c + 1]) - bm));
+          const float2 f = half2_bits_to_float2(ph4[e]);
+          l += f.x + f.y;
+        }
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(pk + canon_off(row, kc, kRowKeys / 8)),
+                     "r"(ph4[0]), "r"(ph4[1]), "r"(ph4[2]), "r"(ph4[3]) : "memory");
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full + 8 * bb);
+
+      if (tt.last && smx) {
+        // ---- piece result: this thread's row, once the piece's last O += P V is done
+        const int s = pos.s, seg = s * p.segs_per_seq + pos.gi, head = pos.gi / p.n_row_tiles;
+        const bool whole = piece_whole && pos.j + 1 == pos.nt;
+        const bool len_ok = device_len(p, s) == pos.L;
+        if (!len_ok && lane == 0) record_error(p.err, PA_ERR_BOUNDS);
+        mbar_wait(kv_empty + 8 * bb, use & 1, p.err, abort);  // O holds tile j
+        __syncwarp();
+        tc_fence_after();
+        const bool real = rg < R;
+        const float lr = (len_ok && real) ? l : 0.f;
+        const int t = real ? rg / kGqa : 0, hl = real ? rg % kGqa : 0;
+        const long long orow = ((long long)s * p.n_qtok + t) * p.n_q_heads + head * kGqa + hl;
+        const int slot = (int)blockIdx.x + seg;
+        float* dst;
+        float inv;
+        if (whole) {
+          dst = p.out + orow * kD;
+          inv = lr > 0.f ? 1.f / lr : 0.f;
+          if (real && p.lse) p.lse[orow] = lr > 0.f ? (m + log2f(lr)) * kLn2 : -INFINITY;
+        } else {
+          dst = p.part_o + ((long long)slot * p.rows_per_seg + row) * kD;
+          inv = len_ok ? 1.f : 0.f;
+          p.part_ml[(long long)slot * p.rows_per_seg + row] = real ? make_float2(m, lr) : make_float2(-INFINITY, 0.f);
+        }
+        const bool store = real || !whole;
+#pragma unroll 1
+        for (int c = 0; c < kD; c += 32) {
+          uint32_t ov[32];
+          tmem_ld32(tO + c, ov);
+          tmem_ld_wait();
+          if (store) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 2)
+              *reinterpret_cast<float2*>(dst + c + dim_of<VT>(i)) =
+                  make_float2(__uint_as_float(ov[i]) * inv, __uint_as_float(ov[i + 1]) * inv);
           }
-          tmem_st_wait();
         }
-        if (raise) {
-          l *= al;
-          m = tmax;
-        }
-        const float bm = (m == -INFINITY) ? 0.f : m;
-#pragma unroll
-        for (int kc = 0; kc < kTile / 8; ++kc) {  // P row, keys 8kc .. 8kc+7
-          uint32_t ph4[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c = 8 * kc + 2 * e;
-            ph4[e] = pack_half2(ex2(__uint_as_float(sv32[c >> 5][c & 31]) - bm),
-                                ex2(__uint_as_float(sv32[(c + 1) >> 5][(c + 1) & 31]) - bm));
-            const float2 f = half2_bits_to_float2(ph4[e]);
-            l += f.x + f.y;
-          }
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(base + SM::kP + canon_off(row, kc, kTile / 8)),
-                       "r"(ph4[0]), "r"(ph4[1]), "r"(ph4[2]), "r"(ph4[3]) : "memory");
-        }
-        fence_proxy_async_smem();
         tc_fence_before();
       }
-      named_bar_sync(kRowBar, kRowThreads);  // P ready (and O rescaled)
-      if (tid == 4 * 32) {  // O += P V
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          tc_mma_f16(tmem + kTcOCol, smem_desc(base + SM::kP + 256 * kk, 128, 1024),
-                     smem_desc(base + SM::kVt + 256 * kk, 128, 1024), kTcIdescO, (jt > jb || kk > 0) ? 1u : 0u);
-        tc_commit(bar_pv);
-      }
-      mbar_wait(bar_pv, nt_done & 1, p.err, abort);  // every tile buffer is free again
-      tc_fence_after();
-      ++nt_done;
-      if (++st == kStages) { st = 0; ph ^= 1; }
+      row_next(p, pos);
     }
-
-    // ---- piece result: this thread's row
-    const bool len_ok = l_dev == L;
-    if (!len_ok && tid == 0) record_error(p.err, PA_ERR_BOUNDS);
-    if (smx) {  // the whole warp reads O (warp-wide loads); real rows store it
-      __syncwarp();
-      const bool real = rg < R;
-      const float lr = (len_ok && real) ? l : 0.f;
-      const int t = real ? rg / kGqa : 0, hl = real ? rg % kGqa : 0;
-      const long long orow = ((long long)s * p.n_qtok + t) * p.n_q_heads + head * kGqa + hl;
-      float* dst;
-      float inv;
-      const int slot = (int)blockIdx.x + seg;
-      if (whole) {
-        dst = p.out + orow * kD;
-        inv = lr > 0.f ? 1.f / lr : 0.f;
-        if (real && p.lse) p.lse[orow] = lr > 0.f ? (m + log2f(lr)) * kLn2 : -INFINITY;
-      } else {
-        dst = p.part_o + ((long long)slot * p.rows_per_seg + row) * kD;
-        inv = len_ok ? 1.f : 0.f;
-        p.part_ml[(long long)slot * p.rows_per_seg + row] = real ? make_float2(m, lr) : make_float2(-INFINITY, 0.f);
-      }
-      const bool store = real || !whole;  // padding rows of a split piece store zeros-weighted partials
-#pragma unroll 1
-      for (int c = 0; c < kD; c += 32) {
-        uint32_t ov[32];
-        tmem_ld32(tO + c, ov);
-        tmem_ld_wait();
-        if (store) {
-#pragma unroll
-          for (int i = 0; i < 32; i += 2)
-            *reinterpret_cast<float2*>(dst + c + dim_of<VT>(i)) =
-                make_float2(__uint_as_float(ov[i]) * inv, __uint_as_float(ov[i + 1]) * inv);
-        }
-      }
-    }
-    tc_fence_before();
-    x += je - jb;
-    pos.j = je - 1;
-    row_next(p, pos);
   }
-  // Every issued tile was waited for above, unless a wait expired (the abort
-  // flag): then wait, with a bound, for the copies and MMAs still in flight
-  // before the stages and tensor memory are released.
-  if (*abort && tid == 0) {
-    drain_ring<kStages>(p, bar_full, abort, (int)((issued - a) % kStages), (uint32_t)(((issued - a) / kStages) & 1),
-                        issued - a);
+  // Every copy and MMA was waited for above, unless a wait expired (the abort
+  // flag): then wait, with a bound, for what is still in flight before the
+  // stages and tensor memory are released.
+  if (*abort && w == kTcMmaWarp && lane == 0) {
+    tc_commit(drain);
+    mbar_wait(drain, 0, p.err, abort, /*honour_abort=*/false);
   }
-  if (*abort && tid == 4 * 32) {
-    tc_commit(bar_drain);
-    mbar_wait(bar_drain, 0, p.err, abort, /*honour_abort=*/false);
+  if (*abort && w == kTcCopyWarp && lane == 0) {
+    const long long n = b - a;
+    for (long long k = n > kStages ? n - kStages : 0; k < n; ++k)
+      mbar_wait(raw_full + 8 * (int)(k % kStages), (uint32_t)((k / kStages) & 1), p.err, abort, false,
+                kWaitTimeoutNs / 8);
   }
   tc_fence_before();
   __syncthreads();
