@@ -11,29 +11,38 @@
 //
 //   segment  = (sequence, KV head, row tile of 128 query rows); its tiles are
 //              the 32-key tiles the row tile's last row sees;
-//   S        = Q K^T    tcgen05.mma M = 128 rows, N = 32 keys, K = 256 dims,
-//                       fp32 in tensor memory (two 32-column buffers);
-//   softmax  one thread per query row: the row's logits come from tensor
-//            memory into registers (no shuffles), causal mask, lazy online
-//            maximum (raised only past 2^8; then that row of O is rescaled in
-//            tensor memory), P as binary16 into shared memory;
+//   S        = Q K^T    tcgen05.mma M = 128 rows, N = 32 keys, K = 256 dims:
+//                       Q from tensor memory, K from shared memory, fp32 in
+//                       tensor memory, as two partial sums (two independent
+//                       accumulation chains, which the tensor core overlaps;
+//                       one chain of dependent N = 32 MMAs runs at a fraction
+//                       of its rate), double-buffered;
+//   softmax  one thread per query row: the row's two partial logit sums come
+//            from tensor memory into registers (no shuffles), causal mask,
+//            lazy online maximum (raised only past 2^8; then that row of O is
+//            rescaled in tensor memory), P as binary16 into shared memory;
 //   O       += P V     tcgen05.mma M = 128 rows, N = 256 dims, K = 32 keys,
 //                       fp32 in tensor memory (256 columns).
 //
+// Tensor memory (512 columns x 128 lanes, lane = query row): O in columns
+// 0-255, Q in 256-383 (two binary16 per column), S in 384-511 (two buffers of
+// two 32-column partial sums).
+//
 // The CTA's warps specialise and run as a pipeline over its key tiles, each
 // hand-off an mbarrier:
-//   warps 0-3  softmax and output, one query row per thread (tensor-memory
-//              lane quarters 0-3);
-//   warps 4-7  dequantisation: eight keys each per tile, K and V into
-//              double-buffered binary16 tiles (and Q at a segment start);
-//   warp 8     issues the MMAs (one thread): S of tile j + 1 goes to the tensor
-//              core before O += P V of tile j, so S is computed while the
-//              softmax of the previous tile runs;
-//   warp 9     streams raw K/V row groups into a ring of stages (bulk copies).
+//   warps 0-3   softmax and output, one query row per thread (tensor-memory
+//               lane quarters 0-3);
+//   warps 4-7   K dequantisation, eight keys each per tile, into one of three
+//               binary16 K buffers; Q into tensor memory at a segment start;
+//   warps 8-11  V dequantisation into one of three V^T buffers;
+//   warp 12     issues the MMAs (one thread): S of tile j + 1 goes to the
+//               tensor core before O += P V of tile j, so S is computed while
+//               the softmax of tile j runs;
+//   warp 13     streams raw K/V row groups into a ring of stages (bulk copies).
 //
-// Operands sit in shared memory in the MMA's canonical no-swizzle K-major
-// layout (core matrices of 8 rows x 16 bytes): Q [rows][dims], K [keys][dims],
-// V^T [dims][keys] and P [rows][keys].  Dequantisation reads the raw quants
+// The shared-memory operands sit in the MMA's canonical no-swizzle K-major
+// layout (core matrices of 8 rows x 16 bytes): K [keys][dims], V^T
+// [dims][keys] and P [rows][keys].  Dequantisation reads the raw quants
 // with ldmatrix (thread 4g+t gets four bytes of key g), converts them in
 // registers and writes core matrices with stmatrix (.trans for V), without
 // bank conflicts.  That fixes a per-format order of the head dims inside each
@@ -43,20 +52,23 @@
 // Precision: Q, P and V (q * d rounded once) are binary16.  Quantised K is
 // kept to about 2^-22: it is split as K = K_hi + K_lo, K_hi = q * d rounded to
 // binary16 and K_lo = q * d - K_hi rounded once (a fused multiply-add), and S
-// takes both products (16 more MMAs per tile, cheap on this tensor core), so
-// large logits carry no K rounding.  Every product is accumulated in fp32.
+// takes both products (the two partial sums), so large logits carry no K
+// rounding.  Every product is accumulated in fp32; the softmax denominator
+// sums the fp32 weights before their rounding to binary16 (a relative
+// difference of at most 2^-11 from the sum of the rounded P).
 #pragma once
 
 #include "pa_rows_impl.cuh"
 
 namespace pa_split {
 
-constexpr uint32_t kTcTmemCols = 512;  // S buffers at columns 0 and 32, O at column 256
-constexpr uint32_t kTcOCol = 256;
+constexpr uint32_t kTcTmemCols = 512;
+constexpr uint32_t kTcOCol = 0, kTcQCol = 256, kTcSCol = 384;  // O, Q, S[2][2] (32 columns each)
 constexpr uint32_t kTcIdescS = idesc_f16_f32(kRowTile, kRowKeys);  // 128 x 32
 constexpr uint32_t kTcIdescO = idesc_f16_f32(kRowTile, kD);        // 128 x 256
-constexpr int kTcSmWarps = 4, kTcDqWarp0 = 4, kTcMmaWarp = 8, kTcCopyWarp = 9;
-constexpr int kRowThreads = 10 * 32;
+constexpr int kTcSmWarp0 = 0, kTcKWarp0 = 4, kTcVWarp0 = 8, kTcMmaWarp = 12, kTcCopyWarp = 13;
+constexpr int kRowThreads = 14 * 32;
+constexpr int kTcNB = 3;  // K and V^T tile buffers in shared memory
 
 template <int KT, int VT>
 struct TcSmem {
@@ -65,19 +77,17 @@ struct TcSmem {
   static constexpr int kKBytes = kRowKeys * kD * 2;  // one K tile [32][256]: 16 KB
   static constexpr int kVBytes = kD * kRowKeys * 2;  // one V^T tile [256][32]: 16 KB
   static constexpr int kPBytes = kRowTile * kRowKeys * 2;  // one P tile [128][32]: 8 KB
-  static constexpr int kBuf = kKBytes * (kKSplit ? 2 : 1) + kVBytes + kPBytes;  // one buffer: K_hi [K_lo] V^T P
-  static constexpr int kQ = 0;                       // Q [128][256]: 64 KB
-  static constexpr int kBuf0 = kQ + kRowTile * kD * 2;
-  static constexpr int kKh = 0, kKl = kKBytes, kVt = kKBytes * (kKSplit ? 2 : 1), kP = kVt + kVBytes;
-  static constexpr int kRing = kBuf0 + 2 * kBuf;
+  static constexpr int kKBuf = kKBytes * (kKSplit ? 2 : 1);
+  static constexpr int kK0 = 0, kV0 = kTcNB * kKBuf, kP0 = kV0 + kTcNB * kVBytes;
+  static constexpr int kRing = kP0 + 2 * kPBytes;
   static constexpr int kFit = (232448 - 1024 - kRing - 512) / kStageBytes;
   static constexpr int kStages = kFit > 4 ? 4 : kFit;
   static_assert(kStages >= 2, "row-tile stage ring does not fit");
   static_assert(kRing % 1024 == 0, "tile alignment");
-  // mbarriers: raw full / empty [kStages], kv full / empty [2], s full / empty
-  // [2], p full [2], drain
+  // mbarriers: raw full / empty [kStages], k full / empty, v full / empty
+  // [kTcNB], s full / empty, p full / empty [2], drain
   static constexpr int kBar = kRing + kStages * kStageBytes;
-  static constexpr int kNBar = 2 * kStages + 8 + 1;
+  static constexpr int kNBar = 2 * kStages + 4 * kTcNB + 8 + 1;
   static constexpr int kMisc = kBar + kNBar * 8;  // abort, start[3], tmem base
   static constexpr int kTotal = kMisc + 32;
   static constexpr int kLaunch = kTotal + 1024;  // the base is aligned to 1024 inside
@@ -195,82 +205,83 @@ __device__ __forceinline__ void tc_dequant_warp(uint32_t region, uint32_t dst, u
 
 // ------------------------------------------------------------------ Q staging
 
-// The row tile's 128 query rows (rows past the 6 * n_qtok real ones are zero)
-// as binary16 in the [rows][dims] tile, each 32-dim window in K's dim order.
-// Task = (row, window): eight float4 loads of the row's 32 dims, four slots out.
+// Row 32 * quarter + lane of the row tile (zero past the 6 * n_qtok real rows)
+// as binary16 into its tensor-memory lane: column c of the 128 holds positions
+// 2c and 2c + 1 of K's dim order (dim_of), the pair of adjacent dims
+// dim_of<KT>(2c), + 1.  taddr: Q's first column, lane field of the quarter.
+// The whole warp calls this.
 template <int KT>
-__device__ __forceinline__ void tc_stage_q(const DecodeParams& p, int s, int head, int rt, uint32_t qsm, int tid) {
-  const int R = kGqa * p.n_qtok;
+__device__ __forceinline__ void tc_stage_q(const DecodeParams& p, int s, int head, int rt, uint32_t taddr, int quarter,
+                                           int lane) {
+  const int row = 32 * quarter + lane, rg = kRowTile * rt + row;
+  const bool real = rg < kGqa * p.n_qtok;
+  const float4* src = reinterpret_cast<const float4*>(
+      p.q + (((long long)s * p.n_qtok + (real ? rg / kGqa : 0)) * p.n_q_heads + head * kGqa + (real ? rg % kGqa : 0)) *
+                kD);
 #pragma unroll 1
-  for (int task = tid; task < kRowTile * (kD / 32); task += 4 * 32) {  // tid: 0 .. 127
-    const int row = task & (kRowTile - 1), win = task >> 7, rg = kRowTile * rt + row;
-    float v[32];
-    if (rg < R) {
-      const float4* src = reinterpret_cast<const float4*>(
-          p.q + (((long long)s * p.n_qtok + rg / kGqa) * p.n_q_heads + head * kGqa + rg % kGqa) * kD + 32 * win);
+  for (int wp = 0; wp < kD / 64; ++wp) {
+    uint32_t h[32];
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      float v[32];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const float4 f = __ldg(src + i);
+        const float4 f = real ? __ldg(src + 8 * (2 * wp + half) + i) : make_float4(0.f, 0.f, 0.f, 0.f);
         v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
       }
-    } else {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = 0.f;
+      for (int c = 0; c < 16; ++c) h[16 * half + c] = pack_half2(v[dim_of<KT>(2 * c)], v[dim_of<KT>(2 * c) + 1]);
     }
-#pragma unroll
-    for (int sl = 0; sl < 4; ++sl) {
-      uint32_t h[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int p0 = 8 * sl + 2 * k;
-        h[k] = pack_half2(v[dim_of<KT>(p0)], v[dim_of<KT>(p0 + 1)]);
-      }
-      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(qsm + canon_off(row, 4 * win + sl, kD / 8)),
-                   "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3]) : "memory");
-    }
+    __syncwarp();
+    tmem_st32(taddr + 32 * wp, h);
   }
+  tmem_st_wait();
 }
 
 // ------------------------------------------------------------------ the kernel
 
 // A tile's place in the CTA's walk, as every role sees it.
 struct TcTile {
-  RowPos pos;    // segment and tile
-  bool first;    // the first tile of a piece (a new segment, or the CTA's first)
-  bool last;     // the last tile of a piece
+  bool first;  // the first tile of a piece (a new segment, or the CTA's first)
+  bool last;   // the last tile of a piece
 };
 
 __device__ __forceinline__ TcTile tc_tile(const RowPos& pos, long long x, long long a, long long b) {
-  return TcTile{pos, x == a || pos.j == 0, x + 1 == b || pos.j + 1 == pos.nt};
+  return TcTile{x == a || pos.j == 0, x + 1 == b || pos.j + 1 == pos.nt};
 }
 
 template <int KT, int VT>
 __global__ void __launch_bounds__(kRowThreads, 1) pa_rows_tc_kernel(const __grid_constant__ DecodeParams p) {
   using SM = TcSmem<KT, VT>;
   using G = RowStageGeo<KT, VT>;
-  constexpr int kStages = SM::kStages;
+  constexpr int kStages = SM::kStages, NB = kTcNB;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
   const uint32_t base = smem_u32(smem);
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
-  const uint32_t bars = base + SM::kBar;
-  const uint32_t raw_full = bars, raw_empty = bars + 8 * kStages;
-  // Hand-offs (b = j & 1 is tile j's buffer, u = j >> 1 its use of it; every
-  // wait below is on a phase that cannot be two ahead of the waiter):
+  // Hand-offs.  Tile j (j-th of the CTA) uses K / V^T buffer kb = j % 3 for
+  // the ku = j / 3-th time and S / P buffer sb = j & 1 for the su = j >> 1-th
+  // time; every wait is on a phase that cannot be two ahead of its waiter.
   //   raw_full / raw_empty  copy warp <-> dequantisation, per ring stage
-  //   kv_full   dequantisation -> MMA: K and V^T of tile j in buffer b
-  //   kv_empty  MMA commit after O += P V of tile j: buffer b free again; also
-  //             "O holds tiles .. j" for the softmax warps
-  //   s_full    MMA commit after S(j); s_empty: softmax has S(j) in registers
-  //   p_full    softmax -> MMA: P of tile j in buffer b
-  const uint32_t kv_full = bars + 16 * kStages, kv_empty = kv_full + 16, s_full = kv_full + 32,
-                 s_empty = kv_full + 48, p_full = kv_full + 64, drain = kv_full + 80;
+  //   k_full / v_full       dequantisation -> MMA (K also means "Q is staged")
+  //   k_empty               MMA commit after S(j): K buffer free, S(j) done
+  //   v_empty               MMA commit after O += P V of tile j: V^T buffer free
+  //   s_full / s_empty      S(j) in tensor memory / in the softmax registers
+  //   p_full / p_empty      P(j) in shared memory / O += P V of tile j done
+  const uint32_t bars = base + SM::kBar;
+  const uint32_t raw_full = bars, raw_empty = raw_full + 8 * kStages;
+  const uint32_t k_full = raw_empty + 8 * kStages, k_empty = k_full + 8 * NB, v_full = k_empty + 8 * NB,
+                 v_empty = v_full + 8 * NB;
+  const uint32_t s_full = v_empty + 8 * NB, s_empty = s_full + 16, p_full = s_empty + 16, p_empty = p_full + 16,
+                 drain = p_empty + 16;
   volatile int* abort = reinterpret_cast<volatile int*>(smem + SM::kMisc);
   int* start = reinterpret_cast<int*>(smem + SM::kMisc + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM::kMisc + 16);
   const uint32_t ring = base + SM::kRing;
-  auto buf = [&](int bb) { return base + SM::kBuf0 + bb * SM::kBuf; };
+  auto kbuf = [&](int kb) { return base + SM::kK0 + kb * SM::kKBuf; };
+  auto vbuf = [&](int kb) { return base + SM::kV0 + kb * SM::kVBytes; };
+  auto pbuf = [&](int sb) { return base + SM::kP0 + sb * SM::kPBytes; };
 
   const long long T = p.total_tiles;
   const int Gn = p.n_ctas;
@@ -281,14 +292,19 @@ __global__ void __launch_bounds__(kRowThreads, 1) pa_rows_tc_kernel(const __grid
     *abort = 0;
     for (int i = 0; i < kStages; ++i) {
       mbar_init(raw_full + 8 * i, 1);
-      mbar_init(raw_empty + 8 * i, 4);
+      mbar_init(raw_empty + 8 * i, 8);  // four K and four V warps
+    }
+    for (int i = 0; i < NB; ++i) {
+      mbar_init(k_full + 8 * i, 4);
+      mbar_init(k_empty + 8 * i, 1);
+      mbar_init(v_full + 8 * i, 4);
+      mbar_init(v_empty + 8 * i, 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(kv_full + 8 * i, 4);
-      mbar_init(kv_empty + 8 * i, 1);
       mbar_init(s_full + 8 * i, 1);
-      mbar_init(s_empty + 8 * i, kTcSmWarps);
-      mbar_init(p_full + 8 * i, kTcSmWarps);
+      mbar_init(s_empty + 8 * i, 4);
+      mbar_init(p_full + 8 * i, 4);
+      mbar_init(p_empty + 8 * i, 1);
     }
     mbar_init(drain, 1);
     fence_mbar_init();
@@ -313,89 +329,129 @@ __global__ void __launch_bounds__(kRowThreads, 1) pa_rows_tc_kernel(const __grid
   pos0.L = any ? p.lens[pos0.s] : 0;
   pos0.nt = any ? row_seg_tiles(p, pos0.L, pos0.gi) : 0;
   const int R = kGqa * p.n_qtok;
+  const int n = (int)(b - a);
 
   if (any && w == kTcCopyWarp) {
     // ---- raw K/V stages
     const uint64_t policy = l2_evict_first_policy();
     RowPos pos = pos0;
-    for (long long x = a; x < b; ++x) {
+    for (int j = 0; j < n; ++j) {
       if (__any_sync(0xffffffffu, *abort != 0)) break;
-      const int j = (int)(x - a), slot = j % kStages, use = j / kStages;
+      const int slot = j % kStages, use = j / kStages;
       if (use > 0) mbar_wait(raw_empty + 8 * slot, (use - 1) & 1, p.err, abort);
       const int tb = row_entry(p, pos, lane);
       issue_stage<KT, VT>(p, pos, tb, ring + slot * G::kBytes, raw_full + 8 * slot, policy, lane);
       row_next(p, pos);
     }
-  } else if (any && w >= kTcDqWarp0 && w < kTcDqWarp0 + 4) {
-    // ---- dequantisation (and Q at every segment start)
-    const int dw = w - kTcDqWarp0, dtid = tid - 32 * kTcDqWarp0;
+  } else if (any && w >= kTcKWarp0 && w < kTcKWarp0 + 4) {
+    // ---- K dequantisation, and Q into tensor memory at every piece start
+    const int dw = w - kTcKWarp0;
     RowPos pos = pos0;
-    for (long long x = a; x < b; ++x) {
-      const TcTile tt = tc_tile(pos, x, a, b);
-      const int j = (int)(x - a), bb = j & 1, use = j >> 1;
+    for (int j = 0; j < n; ++j) {
+      const TcTile tt = tc_tile(pos, a + j, a, b);
+      const int kb = j % NB, ku = j / NB, slot = j % kStages;
       if (tt.first) {
-        // the previous piece's S is done with Q before it is overwritten
-        if (j > 0) mbar_wait(s_full + 8 * ((j - 1) & 1), ((j - 1) >> 1) & 1, p.err, abort);
-        tc_stage_q<KT>(p, pos.s, pos.gi / p.n_row_tiles, pos.gi % p.n_row_tiles, base + SM::kQ, dtid);
+        if (j > 0) {  // S(j - 1), the previous piece's last, is done with Q
+          mbar_wait(k_empty + 8 * ((j - 1) % NB), ((j - 1) / NB) & 1, p.err, abort);
+          __syncwarp();
+          tc_fence_after();
+        }
+        tc_stage_q<KT>(p, pos.s, pos.gi / p.n_row_tiles, pos.gi % p.n_row_tiles,
+                       tmem + kTcQCol + ((uint32_t)(32 * dw) << 16), dw, lane);
       }
-      const int slot = j % kStages;
       mbar_wait(raw_full + 8 * slot, (j / kStages) & 1, p.err, abort);
-      if (use > 0) mbar_wait(kv_empty + 8 * bb, (use - 1) & 1, p.err, abort);  // tile j - 2 is done with it
+      if (ku > 0) mbar_wait(k_empty + 8 * kb, (ku - 1) & 1, p.err, abort);  // S(j - 3) is done with the buffer
       __syncwarp();
       const int n_keys = min(kRowKeys, pos.L - pos.j * kRowKeys);
-      const uint32_t sk = ring + slot * G::kBytes, bk = buf(bb);
-      tc_dequant_warp<KT, false>(sk, bk + SM::kKh, bk + SM::kKl, dw, lane, n_keys);
-      tc_dequant_warp<VT, true>(sk + G::kKBytes, bk + SM::kVt, 0u, dw, lane, n_keys);
+      tc_dequant_warp<KT, false>(ring + slot * G::kBytes, kbuf(kb), kbuf(kb) + SM::kKBytes, dw, lane, n_keys);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(raw_empty + 8 * slot);
+        mbar_arrive(k_full + 8 * kb);
+      }
+      row_next(p, pos);
+    }
+  } else if (any && w >= kTcVWarp0 && w < kTcVWarp0 + 4) {
+    // ---- V dequantisation
+    const int dw = w - kTcVWarp0;
+    RowPos pos = pos0;
+    for (int j = 0; j < n; ++j) {
+      const int kb = j % NB, ku = j / NB, slot = j % kStages;
+      mbar_wait(raw_full + 8 * slot, (j / kStages) & 1, p.err, abort);
+      if (ku > 0) mbar_wait(v_empty + 8 * kb, (ku - 1) & 1, p.err, abort);  // O += P V of tile j - 3 is done with it
+      __syncwarp();
+      const int n_keys = min(kRowKeys, pos.L - pos.j * kRowKeys);
+      tc_dequant_warp<VT, true>(ring + slot * G::kBytes + G::kKBytes, vbuf(kb), 0u, dw, lane, n_keys);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(raw_empty + 8 * slot);
-        mbar_arrive(kv_full + 8 * bb);
+        mbar_arrive(v_full + 8 * kb);
       }
       row_next(p, pos);
     }
   } else if (any && w == kTcMmaWarp) {
-    // ---- MMA issue (one thread): S(j), then O += P V of tile j - 1
-    if (lane == 0) {
-      auto pv = [&](int jj, bool first) {  // O (+)= P V of tile jj
-        const int pb = jj & 1;
-        mbar_wait(p_full + 8 * pb, (jj >> 1) & 1, p.err, abort);
-        tc_fence_after();
-        const uint32_t pk = buf(pb);
+    // ---- MMA issue (the whole warp, one elected lane issuing): S(j), then
+    // O += P V of tile j - 1
+    const uint32_t tq = __shfl_sync(0xffffffffu, tmem, 0), ub = __shfl_sync(0xffffffffu, base, 0);
+    const uint64_t kdesc0 = smem_desc(ub + SM::kK0, 128, 4096), vdesc0 = smem_desc(ub + SM::kV0, 128, 512),
+                   pdesc0 = smem_desc(ub + SM::kP0, 128, 512);
+    // descriptor start addresses count 16-byte units
+    auto pv = [&](int jj, bool first) {
+      const int kb = jj % NB, sb = jj & 1;
+      mbar_wait(v_full + 8 * kb, (jj / NB) & 1, p.err, abort);
+      mbar_wait(p_full + 8 * sb, (jj >> 1) & 1, p.err, abort);
+      __syncwarp();
+      tc_fence_after();
+      const uint64_t pd = pdesc0 + (uint64_t)((sb * SM::kPBytes) >> 4), vd = vdesc0 + (uint64_t)((kb * SM::kVBytes) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < kRowKeys / 16; ++kk)
-          tc_mma_f16(tmem + kTcOCol, smem_desc(pk + SM::kP + 256 * kk, 128, 512),
-                     smem_desc(pk + SM::kVt + 256 * kk, 128, 512), kTcIdescO, (first && kk == 0) ? 0u : 1u);
-        tc_commit(kv_empty + 8 * pb);
-      };
-      RowPos pos = pos0;
-      bool prev_first = false;
-      for (long long x = a; x < b; ++x) {
-        const int j = (int)(x - a), bb = j & 1, use = j >> 1;
-        const bool first = tc_tile(pos, x, a, b).first;
-        mbar_wait(kv_full + 8 * bb, use & 1, p.err, abort);
-        if (use > 0) mbar_wait(s_empty + 8 * bb, (use - 1) & 1, p.err, abort);
-        tc_fence_after();
-        const uint32_t bk = buf(bb), dS = tmem + kRowKeys * bb;
+      for (int kk = 0; kk < kRowKeys / 16; ++kk)
+        tc_mma_f16_warp(tq + kTcOCol, pd + 16 * kk, vd + 16 * kk, kTcIdescO, (first && kk == 0) ? 0u : 1u);
+      tc_commit_warp(v_empty + 8 * kb);
+      tc_commit_warp(p_empty + 8 * sb);
+    };
+    RowPos pos = pos0;
+    bool prev_first = false;
+    for (int j = 0; j < n; ++j) {
+      const int kb = j % NB, sb = j & 1, su = j >> 1;
+      const bool first = tc_tile(pos, a + j, a, b).first;
+      mbar_wait(k_full + 8 * kb, (j / NB) & 1, p.err, abort);
+      if (su > 0) mbar_wait(s_empty + 8 * sb, (su - 1) & 1, p.err, abort);
+      __syncwarp();
+      tc_fence_after();
+      // two chains: Q K_hi^T and Q K_lo^T, or (binary16 K) the two halves of the dims
+      const uint32_t dA = tq + kTcSCol + 2 * kRowKeys * sb, dB = dA + kRowKeys;
+      const uint64_t kd = kdesc0 + (uint64_t)((kb * SM::kKBuf) >> 4);
+      if (SM::kKSplit) {
 #pragma unroll
-        for (int ks = 0; ks < kD / 16; ++ks)
-          tc_mma_f16(dS, smem_desc(base + SM::kQ + 256 * ks, 128, 4096), smem_desc(bk + SM::kKh + 256 * ks, 128, 4096),
-                     kTcIdescS, ks > 0);
-        if (SM::kKSplit) {
-#pragma unroll
-          for (int ks = 0; ks < kD / 16; ++ks)
-            tc_mma_f16(dS, smem_desc(base + SM::kQ + 256 * ks, 128, 4096),
-                       smem_desc(bk + SM::kKl + 256 * ks, 128, 4096), kTcIdescS, 1);
+        for (int ks = 0; ks < kD / 16; ++ks) {
+          tc_mma_f16_tmem_a_warp(dA, tq + kTcQCol + 8 * ks, kd + 16 * ks, kTcIdescS, ks > 0);
+          tc_mma_f16_tmem_a_warp(dB, tq + kTcQCol + 8 * ks, kd + (SM::kKBytes >> 4) + 16 * ks, kTcIdescS, ks > 0);
         }
-        tc_commit(s_full + 8 * bb);
-        if (j > 0) pv(j - 1, prev_first);
-        prev_first = first;
-        row_next(p, pos);
+      } else {
+#pragma unroll
+        for (int ks = 0; ks < kD / 32; ++ks) {
+          tc_mma_f16_tmem_a_warp(dA, tq + kTcQCol + 8 * ks, kd + 16 * ks, kTcIdescS, ks > 0);
+          tc_mma_f16_tmem_a_warp(dB, tq + kTcQCol + 8 * (ks + kD / 32), kd + 16 * (ks + kD / 32), kTcIdescS, ks > 0);
+        }
       }
-      if (b > a) pv((int)(b - a) - 1, prev_first);
+      tc_commit_warp(k_empty + 8 * kb);
+      tc_commit_warp(s_full + 8 * sb);
+      if (j > 0) pv(j - 1, prev_first);
+      prev_first = first;
+      row_next(p, pos);
     }
+    if (n > 0) pv(n - 1, prev_first);
+    // the last commits have arrived before the CTA's barriers go away
+    for (int jj = max(0, n - NB); jj < n; ++jj) {
+      mbar_wait(k_empty + 8 * (jj % NB), (jj / NB) & 1, p.err, abort);
+      mbar_wait(v_empty + 8 * (jj % NB), (jj / NB) & 1, p.err, abort);
+    }
+    for (int jj = max(0, n - 2); jj < n; ++jj) mbar_wait(p_empty + 8 * (jj & 1), (jj >> 1) & 1, p.err, abort);
     __syncwarp();
-  } else if (any && w < kTcSmWarps) {
+  } else if (any && w < kTcSmWarp0 + 4) {
     // ---- softmax and output: one query row per thread
     const int row = 32 * w + lane;
     const uint32_t t_lane = (uint32_t)(32 * w) << 16;
@@ -405,9 +461,9 @@ __global__ void __launch_bounds__(kRowThreads, 1) pa_rows_tc_kernel(const __grid
     float m = -INFINITY, l = 0.f;
     int vis = -1, piece_j0 = 0;
     bool piece_whole = false;
-    for (long long x = a; x < b; ++x) {
-      const TcTile tt = tc_tile(pos, x, a, b);
-      const int j = (int)(x - a), bb = j & 1, use = j >> 1;
+    for (int j = 0; j < n; ++j) {
+      const TcTile tt = tc_tile(pos, a + j, a, b);
+      const int sb = j & 1, su = j >> 1;
       const int rt = pos.gi % p.n_row_tiles, rg = kRowTile * rt + row;
       const bool smx = kRowTile * rt + 32 * w < R;  // the warp holds a real row
       if (tt.first) {
@@ -418,31 +474,39 @@ __global__ void __launch_bounds__(kRowThreads, 1) pa_rows_tc_kernel(const __grid
         piece_whole = pos.j == 0;
       }
       const int k0 = pos.j * kRowKeys;
-      // S of tile j: into registers, then the buffer is free for S(j + 2)
-      mbar_wait(s_full + 8 * bb, use & 1, p.err, abort);
+      // S(j) (the sum of its two partials) into registers; the buffer is then
+      // free for S(j + 2)
+      mbar_wait(s_full + 8 * sb, su & 1, p.err, abort);
       __syncwarp();
       tc_fence_after();
-      uint32_t sv[32];
-      tmem_ld32(tmem + t_lane + kRowKeys * bb, sv);
+      uint32_t sa[32], sv[32];
+      tmem_ld32(tmem + t_lane + kTcSCol + 2 * kRowKeys * sb, sa);
+      tmem_ld32(tmem + t_lane + kTcSCol + 2 * kRowKeys * sb + kRowKeys, sv);
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(s_empty + 8 * bb);
-      float tmax = -INFINITY;
+      if (lane == 0) mbar_arrive(s_empty + 8 * sb);
+      float x[32];
 #pragma unroll
-      for (int c = 0; c < kRowKeys; ++c) {
-        const float v = (k0 + c <= vis) ? __uint_as_float(sv[c]) * scale_log2 : -INFINITY;
-        sv[c] = __float_as_uint(v);
-        tmax = fmaxf(tmax, v);
+      for (int c = 0; c < kRowKeys; ++c) x[c] = __uint_as_float(sa[c]) + __uint_as_float(sv[c]);
+      if (k0 + kRowKeys - 1 > vis) {  // the causal edge (or padding rows): mask
+#pragma unroll
+        for (int c = 0; c < kRowKeys; ++c)
+          if (k0 + c > vis) x[c] = -INFINITY;
       }
+      float mx[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) mx[c] = fmaxf(fmaxf(x[c], x[c + 8]), fmaxf(x[c + 16], x[c + 24]));
+      const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) *
+                         scale_log2;
       // Lazy maximum: raised (rarely, after a row's first tile) past 2^8.  The
-      // rows of O that hold weight are rescaled in tensor memory once the
-      // previous O += P V is done; the tensor-memory loads and stores are
-      // warp-wide, so the whole warp runs them when any of its rows rises.
+      // row of O is rescaled in tensor memory once O += P V of tile j - 1 is
+      // done; tensor-memory loads and stores are warp-wide, so the whole warp
+      // runs them when any of its rows rises.
       const bool raise = tmax > m + kLazy;
       const float al = raise ? ((m == -INFINITY) ? 1.f : ex2(m - tmax)) : 1.f;
       if (smx && __any_sync(0xffffffffu, raise) && j > piece_j0) {
-        mbar_wait(kv_empty + 8 * ((j - 1) & 1), ((j - 1) >> 1) & 1, p.err, abort);  // O holds tile j - 1
+        mbar_wait(p_empty + 8 * ((j - 1) & 1), ((j - 1) >> 1) & 1, p.err, abort);
         __syncwarp();
         tc_fence_after();
 #pragma unroll 1
@@ -460,27 +524,26 @@ __global__ void __launch_bounds__(kRowThreads, 1) pa_rows_tc_kernel(const __grid
         l *= al;
         m = tmax;
       }
-      // P of tile j into buffer bb, once tile j - 2's O += P V is done with it
-      if (use > 0) mbar_wait(kv_empty + 8 * bb, (use - 1) & 1, p.err, abort);
-      const float bm = (m == -INFINITY) ? 0.f : m;
-      const uint32_t pk = buf(bb) + SM::kP;
+      const float nbm = (m == -INFINITY) ? 0.f : -m;
+      uint32_t ph[16];
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int kc = 0; kc < kRowKeys / 8; ++kc) {
-        uint32_t ph4[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int c = 8 * kc + 2 * e;
-          ph4[e] = pack_half2(ex2(__uint_as_float(sv[c]) - bm), ex2(__uint_as_float(sv[c + 1]) - bm));
-          const float2 f = half2_bits_to_float2(ph4[e]);
-          l += f.x + f.y;
-        }
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(pk + canon_off(row, kc, kRowKeys / 8)),
-                     "r"(ph4[0]), "r"(ph4[1]), "r"(ph4[2]), "r"(ph4[3]) : "memory");
+      for (int c = 0; c < 16; ++c) {
+        const float e0 = ex2(fmaf(x[2 * c], scale_log2, nbm)), e1 = ex2(fmaf(x[2 * c + 1], scale_log2, nbm));
+        ls[c & 3] += e0 + e1;
+        ph[c] = pack_half2(e0, e1);
       }
+      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      // P(j) into shared-memory buffer sb once O += P V of tile j - 2 has read it
+      if (su > 0) mbar_wait(p_empty + 8 * sb, (su - 1) & 1, p.err, abort);
+      const uint32_t pk = pbuf(sb);
+#pragma unroll
+      for (int kc = 0; kc < kRowKeys / 8; ++kc)
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(pk + canon_off(row, kc, kRowKeys / 8)),
+                     "r"(ph[4 * kc]), "r"(ph[4 * kc + 1]), "r"(ph[4 * kc + 2]), "r"(ph[4 * kc + 3]) : "memory");
       fence_proxy_async_smem();
-      tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full + 8 * bb);
+      if (lane == 0) mbar_arrive(p_full + 8 * sb);
 
       if (tt.last && smx) {
         // ---- piece result: this thread's row, once the piece's last O += P V is done
@@ -488,7 +551,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) pa_rows_tc_kernel(const __grid
         const bool whole = piece_whole && pos.j + 1 == pos.nt;
         const bool len_ok = device_len(p, s) == pos.L;
         if (!len_ok && lane == 0) record_error(p.err, PA_ERR_BOUNDS);
-        mbar_wait(kv_empty + 8 * bb, use & 1, p.err, abort);  // O holds tile j
+        mbar_wait(p_empty + 8 * sb, su & 1, p.err, abort);
         __syncwarp();
         tc_fence_after();
         const bool real = rg < R;
@@ -528,15 +591,13 @@ __global__ void __launch_bounds__(kRowThreads, 1) pa_rows_tc_kernel(const __grid
   // Every copy and MMA was waited for above, unless a wait expired (the abort
   // flag): then wait, with a bound, for what is still in flight before the
   // stages and tensor memory are released.
-  if (*abort && w == kTcMmaWarp && lane == 0) {
-    tc_commit(drain);
+  if (w == kTcMmaWarp && __any_sync(0xffffffffu, *abort != 0)) {  // the lane that issued the MMAs commits
+    tc_commit_warp(drain);
     mbar_wait(drain, 0, p.err, abort, /*honour_abort=*/false);
   }
   if (*abort && w == kTcCopyWarp && lane == 0) {
-    const long long n = b - a;
-    for (long long k = n > kStages ? n - kStages : 0; k < n; ++k)
-      mbar_wait(raw_full + 8 * (int)(k % kStages), (uint32_t)((k / kStages) & 1), p.err, abort, false,
-                kWaitTimeoutNs / 8);
+    for (int k = n > kStages ? n - kStages : 0; k < n; ++k)
+      mbar_wait(raw_full + 8 * (k % kStages), (uint32_t)((k / kStages) & 1), p.err, abort, false, kWaitTimeoutNs / 8);
   }
   tc_fence_before();
   __syncthreads();
