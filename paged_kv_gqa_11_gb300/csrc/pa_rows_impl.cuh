@@ -6,7 +6,7 @@
 // than a chunked prefill up to 96 query tokens (llama.cpp fork PR #2, the
 // commit on KV-streaming ubatches of more than 8 tokens).  With 6 * n_qtok
 // query rows per KV head the rows are the MMA's M dimension: a segment is
-// (sequence, KV head, row tile of 128 rows), and its tiles are the 32-key tiles
+// (sequence, KV head, row tile of 128 rows), and its tiles are the 64-key tiles
 // its last row can see, so early row tiles of a long verify batch stop short of
 // the newest keys.  Segments are cut into pieces by the same stream-K planner as
 // the decode kernels and merged by the same LSE merge.
@@ -17,22 +17,22 @@
 namespace pa_split {
 
 constexpr int kRowTile = 128;                  // query rows per row tile
-constexpr int kRowKeys = 32;                   // keys per row-tile key tile (two row groups)
+constexpr int kRowKeys = 64;                   // keys per row-tile key tile
+constexpr int kStageKeys = 32;                 // keys per copy stage (two row groups); two stages per tile
 constexpr int kMaxRowsQTok = 96;               // query tokens the row tiles take
 
-// A stage of one key tile: its two K row groups, then its two V row groups.
+// A K stage holds two K row groups (half a key tile); a V stage the same two
+// V row groups.  K and V stages are separate rings.
 template <int KT, int VT>
 struct RowStageGeo {
-  static constexpr int kKGroup = pa_layout::group_bytes<KT>();
-  static constexpr int kVGroup = pa_layout::group_bytes<VT>();
-  static constexpr int kKBytes = 2 * kKGroup;
-  static constexpr int kBytes = 2 * (kKGroup + kVGroup);
+  static constexpr int kKBytes = 2 * pa_layout::group_bytes<KT>();
+  static constexpr int kVBytes = 2 * pa_layout::group_bytes<VT>();
 };
 
 // ------------------------------------------------------------------ the walk
 
 // Tiles of segment gi (KV head gi / n_row_tiles, row tile gi % n_row_tiles) of
-// a sequence of length L: the 32-key tiles that the tile's last row sees.
+// a sequence of length L: the 64-key tiles that the tile's last row sees.
 __device__ __forceinline__ int row_seg_tiles(const DecodeParams& p, int L, int gi) {
   const int rt = gi % p.n_row_tiles;
   const int t_last = min(p.n_qtok - 1, (kRowTile * (rt + 1) - 1) / kGqa);
@@ -77,26 +77,27 @@ __device__ __forceinline__ void row_next(const DecodeParams& p, RowPos& t) {
 
 // ------------------------------------------------------------------ stage copies
 
-// Table entry of row group `lane` (0..1) of key tile t, or -1 for lanes past
-// the tile's row groups.
-__device__ __forceinline__ int row_entry(const DecodeParams& p, const RowPos& t, int lane) {
-  const int k0 = t.j * kRowKeys, n = min(kRowKeys, t.L - k0);
+// Table entry of row group `lane` (0..1) of stage `half` (0..1) of key tile
+// t, or -1 for lanes past the stage's row groups.
+__device__ __forceinline__ int row_entry(const DecodeParams& p, const RowPos& t, int half, int lane) {
+  const int k0 = t.j * kRowKeys + half * kStageKeys, n = min(kStageKeys, t.L - k0);
   if (lane >= 2 || lane * kGroup >= n || t.s >= p.n_seq) return -1;
   return __ldg(p.table + (long long)t.s * p.table_stride + (k0 + lane * kGroup) / p.page_size);
 }
 
-// Fill one stage with key tile t (two row groups of one KV head, K then V);
+// Fill one stage with half `half` of key tile t: its two row groups of one KV
+// head from the K pool (kIsV false, format T = the K format) or the V pool;
 // tb: this lane's table entry (row_entry).  Groups past the sequence's last
-// key are not copied; a group whose entry is outside the pool is zero-filled
-// and reported.  The whole warp calls this.
-template <int KT, int VT>
-__device__ __forceinline__ void issue_stage(const DecodeParams& p, const RowPos& t, int tb, uint32_t sk, uint32_t fb,
-                                            uint64_t policy, int lane) {
-  using G = RowStageGeo<KT, VT>;
-  constexpr int RK = Fmt<KT>::kRow, RV = Fmt<VT>::kRow;
+// key are not copied (a stage wholly past it completes with no bytes); a group
+// whose entry is outside the pool is zero-filled and reported.  The whole warp
+// calls this.
+template <int T, bool kIsV>
+__device__ __forceinline__ void issue_half(const DecodeParams& p, const RowPos& t, int half, int tb, uint32_t dst,
+                                           uint32_t fb, uint64_t policy, int lane) {
+  constexpr int GB = pa_layout::group_bytes<T>(), RB = Fmt<T>::kRow;
   const int head = t.gi / p.n_row_tiles;
-  const int k0 = t.j * kRowKeys, n = min(kRowKeys, t.L - k0), ng = (n + kGroup - 1) / kGroup;
-  const uint32_t sv = sk + G::kKBytes;
+  const int k0 = t.j * kRowKeys + half * kStageKeys, n = min(kStageKeys, t.L - k0);
+  const int ng = n > 0 ? (n + kGroup - 1) / kGroup : 0;
   const bool mine = lane < ng;
   const bool ok = !mine || (tb >= 0 && tb < p.n_blocks);
   const unsigned bad = __ballot_sync(0xffffffffu, !ok);
@@ -104,19 +105,17 @@ __device__ __forceinline__ void issue_stage(const DecodeParams& p, const RowPos&
     if (lane == 0) record_error(p.err, PA_ERR_BOUNDS);
     for (int q = 0; q < 2; ++q) {
       if (!((bad >> q) & 1)) continue;
-      for (int i = lane; i < G::kKGroup / 16; i += 32) sts128_zero(sk + q * G::kKGroup + 16 * i);
-      for (int i = lane; i < G::kVGroup / 16; i += 32) sts128_zero(sv + q * G::kVGroup + 16 * i);
+      for (int i = lane; i < GB / 16; i += 32) sts128_zero(dst + q * GB + 16 * i);
     }
     fence_proxy_async_smem();
   }
   const int n_good = __popc(__ballot_sync(0xffffffffu, mine && ok));
   __syncwarp();
-  if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)n_good * (G::kKGroup + G::kVGroup));
+  if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)n_good * GB);
   __syncwarp();
   if (mine && ok) {
     const long long row = ((long long)tb * p.n_kv_heads + head) * p.page_size + (k0 + lane * kGroup) % p.page_size;
-    bulk_g2s_hint(sk + lane * G::kKGroup, p.k_pool + row * RK, G::kKGroup, fb, policy);
-    bulk_g2s_hint(sv + lane * G::kVGroup, p.v_pool + row * RV, G::kVGroup, fb, policy);
+    bulk_g2s_hint(dst + lane * GB, (kIsV ? p.v_pool : p.k_pool) + row * RB, GB, fb, policy);
   }
   __syncwarp();
 }

@@ -10,35 +10,37 @@
 // dense contraction, so it runs on tcgen05:
 //
 //   segment  = (sequence, KV head, row tile of 128 query rows); its tiles are
-//              the 32-key tiles the row tile's last row sees;
-//   S        = Q K^T    tcgen05.mma M = 128 rows, N = 32 keys, K = 256 dims:
+//              the 64-key tiles the row tile's last row sees;
+//   S        = Q K^T    tcgen05.mma M = 128 rows, N = 64 keys, K = 256 dims:
 //                       Q from tensor memory, K from shared memory, fp32 in
-//                       tensor memory, as two partial sums (two independent
-//                       accumulation chains, which the tensor core overlaps;
-//                       one chain of dependent N = 32 MMAs runs at a fraction
-//                       of its rate), double-buffered;
-//   softmax  one thread per query row: the row's two partial logit sums come
-//            from tensor memory into registers (no shuffles), causal mask,
-//            lazy online maximum (raised only past 2^8; then that row of O is
-//            rescaled in tensor memory), P as binary16 into shared memory;
-//   O       += P V     tcgen05.mma M = 128 rows, N = 256 dims, K = 32 keys,
+//                       tensor memory, double-buffered;
+//   softmax  one thread per query row: the row's logits come from tensor
+//            memory into registers (no shuffles), causal mask, lazy online
+//            maximum (raised only past 2^8; then that row of O is rescaled in
+//            tensor memory), P as binary16 into shared memory;
+//   O       += P V     tcgen05.mma M = 128 rows, N = 256 dims, K = 64 keys,
 //                       fp32 in tensor memory (256 columns).
 //
-// Tensor memory (512 columns x 128 lanes, lane = query row): O in columns
-// 0-255, Q in 256-383 (two binary16 per column), S in 384-511 (two buffers of
-// two 32-column partial sums).
+// An MMA with N of 64 or less costs the tensor core about the same time
+// whatever N is (the issue, not the arithmetic, sets it), so a key tile is as
+// wide as shared memory allows: 64 keys, with K and S double-buffered and V^T
+// and P single.  Tensor memory (512 columns x 128 lanes, lane = query row): O
+// in columns 0-255, Q in 256-383 (two binary16 per column), S in 384-511.
 //
 // The CTA's warps specialise and run as a pipeline over its key tiles, each
 // hand-off an mbarrier:
 //   warps 0-3   softmax and output, one query row per thread (tensor-memory
 //               lane quarters 0-3);
-//   warps 4-7   K dequantisation, eight keys each per tile, into one of three
+//   warps 4-7   K dequantisation, sixteen keys each per tile, into one of two
 //               binary16 K buffers; Q into tensor memory at a segment start;
-//   warps 8-11  V dequantisation into one of three V^T buffers;
+//   warps 8-11  V dequantisation into the V^T buffer, sixteen keys each;
 //   warp 12     issues the MMAs (one thread): S of tile j + 1 goes to the
 //               tensor core before O += P V of tile j, so S is computed while
 //               the softmax of tile j runs;
-//   warp 13     streams raw K/V row groups into a ring of stages (bulk copies).
+//   warps 13-14 stream raw K (warp 13) and V (warp 14) row groups into two
+//               rings of 32-key stages (bulk copies), two stages per key
+//               tile; separate rings let K run ahead of V, which waits for
+//               the previous tile's O += P V.
 //
 // The shared-memory operands sit in the MMA's canonical no-swizzle K-major
 // layout (core matrices of 8 rows x 16 bytes): K [keys][dims], V^T
@@ -52,7 +54,7 @@
 // Precision: Q, P and V (q * d rounded once) are binary16.  Quantised K is
 // kept to about 2^-22: it is split as K = K_hi + K_lo, K_hi = q * d rounded to
 // binary16 and K_lo = q * d - K_hi rounded once (a fused multiply-add), and S
-// takes both products (the two partial sums), so large logits carry no K
+// takes both products (32 MMAs per tile), so large logits carry no K
 // rounding.  Every product is accumulated in fp32; the softmax denominator
 // sums the fp32 weights before their rounding to binary16 (a relative
 // difference of at most 2^-11 from the sum of the rounded P).
@@ -63,35 +65,40 @@
 namespace pa_split {
 
 constexpr uint32_t kTcTmemCols = 512;
-constexpr uint32_t kTcOCol = 0, kTcQCol = 256, kTcSCol = 384;  // O, Q, S[2][2] (32 columns each)
+constexpr uint32_t kTcOCol = 0, kTcQCol = 256, kTcSCol = 384;  // O, Q, S[2] (64 columns each)
 constexpr uint32_t kTcIdescS = idesc_f16_f32(kRowTile, kRowKeys);  // 128 x 32
 constexpr uint32_t kTcIdescO = idesc_f16_f32(kRowTile, kD);        // 128 x 256
-constexpr int kTcSmWarp0 = 0, kTcKWarp0 = 4, kTcVWarp0 = 8, kTcMmaWarp = 12, kTcCopyWarp = 13;
-constexpr int kRowThreads = 14 * 32;
-constexpr int kTcNB = 3;  // K and V^T tile buffers in shared memory
+constexpr int kTcSmWarp0 = 0, kTcKWarp0 = 4, kTcVWarp0 = 8, kTcMmaWarp = 12, kTcCopyK = 13, kTcCopyV = 14;
+constexpr int kRowThreads = 15 * 32;
 
 template <int KT, int VT>
 struct TcSmem {
   static constexpr bool kKSplit = KT != PA_F16;  // K_hi and K_lo
-  static constexpr int kStageBytes = RowStageGeo<KT, VT>::kBytes;
-  static constexpr int kKBytes = kRowKeys * kD * 2;  // one K tile [32][256]: 16 KB
-  static constexpr int kVBytes = kD * kRowKeys * 2;  // one V^T tile [256][32]: 16 KB
-  static constexpr int kPBytes = kRowTile * kRowKeys * 2;  // one P tile [128][32]: 8 KB
-  static constexpr int kKBuf = kKBytes * (kKSplit ? 2 : 1);
-  static constexpr int kK0 = 0, kV0 = kTcNB * kKBuf, kP0 = kV0 + kTcNB * kVBytes;
-  static constexpr int kRing = kP0 + 2 * kPBytes;
-  static constexpr int kFit = (232448 - 1024 - kRing - 512) / kStageBytes;
-  static constexpr int kStages = kFit > 4 ? 4 : kFit;
-  static_assert(kStages >= 2, "row-tile stage ring does not fit");
+  static constexpr int kKStage = RowStageGeo<KT, VT>::kKBytes, kVStage = RowStageGeo<KT, VT>::kVBytes;
+  static constexpr int kKBytes = kRowKeys * kD * 2;         // one K tile [64][256]: 32 KB
+  static constexpr int kVBytes = kD * kRowKeys * 2;         // the V^T tile [256][64]: 32 KB
+  static constexpr int kPBytes = kRowTile * kRowKeys * 2;   // the P tile [128][64]: 16 KB
+  static constexpr int kKBuf = kKBytes * (kKSplit ? 2 : 1);  // K_hi [K_lo]
+  static constexpr int kK0 = 0, kV0 = 2 * kKBuf, kP0 = kV0 + kVBytes;
+  static constexpr int kRing = kP0 + kPBytes;
+  // raw stages: three K stages first if they fit beside a V stage, then as many
+  // V stages as fit (at most four), then K stages up to four
+  static constexpr int kRoom = 232448 - 1024 - kRing - 512;
+  static constexpr int kVFit = (kRoom - 3 * kKStage) / kVStage;
+  static constexpr int kVStages = kVFit >= 1 ? (kVFit > 4 ? 4 : kVFit) : (kRoom - 2 * kKStage) / kVStage;
+  static constexpr int kKFit = (kRoom - kVStages * kVStage) / kKStage;
+  static constexpr int kKStages = kKFit > 4 ? 4 : kKFit;
+  static_assert(kKStages >= 2 && kVStages >= 1, "row-tile stage rings do not fit");
   static_assert(kRing % 1024 == 0, "tile alignment");
-  // mbarriers: raw full / empty [kStages], k full / empty, v full / empty
-  // [kTcNB], s full / empty, p full / empty [2], drain
-  static constexpr int kBar = kRing + kStages * kStageBytes;
-  static constexpr int kNBar = 2 * kStages + 4 * kTcNB + 8 + 1;
+  static constexpr int kVRing = kRing + kKStages * kKStage;
+  // mbarriers: K raw full / empty [kKStages], V raw full / empty [kVStages],
+  // k full / empty [2], v full, s full / empty [2], p full, pv done, drain
+  static constexpr int kBar = kVRing + kVStages * kVStage;
+  static constexpr int kNBar = 2 * kKStages + 2 * kVStages + 4 + 1 + 4 + 1 + 1 + 1;
   static constexpr int kMisc = kBar + kNBar * 8;  // abort, start[3], tmem base
   static constexpr int kTotal = kMisc + 32;
   static constexpr int kLaunch = kTotal + 1024;  // the base is aligned to 1024 inside
-  static_assert(kTotal - kRing - kStages * kStageBytes <= 512, "barrier area");
+  static_assert(kTotal - kBar <= 512, "barrier area");
 };
 
 // Canonical K-major offsets (bytes): operand with `kslots` 8-element slots
@@ -113,9 +120,10 @@ __host__ __device__ constexpr int dim_of(int p) {
 
 // ------------------------------------------------------------------ dequantisation by ldmatrix / stmatrix
 
-// Store four fragment matrices of slots s0 .. s0+3 (8 dims each) of the warp's
-// eight keys: K as rows of the [keys][dims] tile, V transposed into the
-// [dims][keys] tile.  Lane 8j + r gives the address of row r of matrix j.
+// Store four fragment matrices of slots s0 .. s0+3 (8 dims each) of eight
+// keys: K as rows 8w .. 8w+7 of the [keys][dims] tile, V transposed into key
+// slot w of the [dims][keys] tile.  Lane 8j + r gives the address of row r of
+// matrix j.
 template <bool kRoleV>
 __device__ __forceinline__ void tc_store4(uint32_t dst, int w, int lane, int s0, uint32_t r0, uint32_t r1, uint32_t r2,
                                           uint32_t r3) {
@@ -132,12 +140,14 @@ __device__ __forceinline__ uint32_t tc_lo(uint32_t v, uint32_t d2, uint32_t hi) 
 }
 
 // Eight keys (8w .. 8w+7) of a raw 32-key stage region of format T (two row
-// groups), as binary16 core matrices: V values q * d into the V^T
-// tile (kRoleV), K exact for F16 or as K_hi / K_lo tiles for Q8_0 and Q4_0.
-// Keys at or past n_keys are written as zeros.
+// groups), as binary16 core matrices: V values q * d into key slot `ds` of
+// the V^T tile (kRoleV), K exact for F16 or as K_hi / K_lo rows 8w .. 8w+7 of
+// the tiles at dst / dst_lo for Q8_0 and Q4_0.  Keys at or past n_keys are
+// written as zeros.
 template <int T, bool kRoleV>
-__device__ __forceinline__ void tc_dequant_warp(uint32_t region, uint32_t dst, uint32_t dst_lo, int w, int lane,
+__device__ __forceinline__ void tc_dequant_warp(uint32_t region, uint32_t dst, uint32_t dst_lo, int w, int ds, int lane,
                                                 int n_keys) {
+  const int dw = kRoleV ? ds : w;  // the store's row group (K) or key slot (V)
   constexpr int C = Fmt<T>::kRowQ / 16;  // 16-byte chunks per row: 32 / 16 / 8
   constexpr int GB = pa_layout::group_bytes<T>();
   // this lane's ldmatrix row: key 8w + (lane & 7) of matrix lane >> 3
@@ -159,7 +169,7 @@ __device__ __forceinline__ void tc_dequant_warp(uint32_t region, uint32_t dst, u
     ldsm_x4(lrow + (((4 * i + (lane >> 3)) ^ (lr & 7)) << 4), x);
     if constexpr (T == PA_F16) {  // chunk = slot, natural order
       if (!live) x[0] = x[1] = x[2] = x[3] = 0u;
-      tc_store4<kRoleV>(dst, w, lane, 4 * i, x[0], x[1], x[2], x[3]);
+      tc_store4<kRoleV>(dst, dw, lane, 4 * i, x[0], x[1], x[2], x[3]);
     } else if constexpr (T == PA_Q8_0) {
       // chunk c = 4i + j: dims 16c + 4t, +1 -> slot 2c; 16c + 4t + 2, +3 -> slot 2c + 1
       uint32_t h[8], l[8];
@@ -174,11 +184,11 @@ __device__ __forceinline__ void tc_dequant_warp(uint32_t region, uint32_t dst, u
           if (!kRoleV) l[2 * j + e] = tc_lo(v, d2, h[2 * j + e]);
         }
       }
-      tc_store4<kRoleV>(dst, w, lane, 8 * i, h[0], h[1], h[2], h[3]);
-      tc_store4<kRoleV>(dst, w, lane, 8 * i + 4, h[4], h[5], h[6], h[7]);
+      tc_store4<kRoleV>(dst, dw, lane, 8 * i, h[0], h[1], h[2], h[3]);
+      tc_store4<kRoleV>(dst, dw, lane, 8 * i + 4, h[4], h[5], h[6], h[7]);
       if (!kRoleV) {
-        tc_store4<false>(dst_lo, w, lane, 8 * i, l[0], l[1], l[2], l[3]);
-        tc_store4<false>(dst_lo, w, lane, 8 * i + 4, l[4], l[5], l[6], l[7]);
+        tc_store4<false>(dst_lo, dw, lane, 8 * i, l[0], l[1], l[2], l[3]);
+        tc_store4<false>(dst_lo, dw, lane, 8 * i + 4, l[4], l[5], l[6], l[7]);
       }
     } else {  // Q4_0: block c = 4i + j; byte b holds dims b (low nibble) and b + 16 (high)
 #pragma unroll
@@ -196,8 +206,8 @@ __device__ __forceinline__ void tc_dequant_warp(uint32_t region, uint32_t dst, u
           if (!kRoleV) l[e] = tc_lo(v[e], d2, h[e]);
         }
         const int c = 4 * i + j;
-        tc_store4<kRoleV>(dst, w, lane, 4 * c, h[0], h[1], h[2], h[3]);
-        if (!kRoleV) tc_store4<false>(dst_lo, w, lane, 4 * c, l[0], l[1], l[2], l[3]);
+        tc_store4<kRoleV>(dst, dw, lane, 4 * c, h[0], h[1], h[2], h[3]);
+        if (!kRoleV) tc_store4<false>(dst_lo, dw, lane, 4 * c, l[0], l[1], l[2], l[3]);
       }
     }
   }
@@ -253,35 +263,32 @@ __device__ __forceinline__ TcTile tc_tile(const RowPos& pos, long long x, long l
 template <int KT, int VT>
 __global__ void __launch_bounds__(kRowThreads, 1) pa_rows_tc_kernel(const __grid_constant__ DecodeParams p) {
   using SM = TcSmem<KT, VT>;
-  using G = RowStageGeo<KT, VT>;
-  constexpr int kStages = SM::kStages, NB = kTcNB;
+  constexpr int kKS = SM::kKStages, kVS = SM::kVStages;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
   const uint32_t base = smem_u32(smem);
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
-  // Hand-offs.  Tile j (j-th of the CTA) uses K / V^T buffer kb = j % 3 for
-  // the ku = j / 3-th time and S / P buffer sb = j & 1 for the su = j >> 1-th
-  // time; every wait is on a phase that cannot be two ahead of its waiter.
-  //   raw_full / raw_empty  copy warp <-> dequantisation, per ring stage
-  //   k_full / v_full       dequantisation -> MMA (K also means "Q is staged")
-  //   k_empty               MMA commit after S(j): K buffer free, S(j) done
-  //   v_empty               MMA commit after O += P V of tile j: V^T buffer free
+  // Hand-offs.  Tile j (the j-th of the CTA) uses K and S buffer kb = j & 1 for
+  // the ku = j >> 1-th time; its stages are 2j and 2j + 1.  Every wait is on a
+  // phase that cannot be two ahead of its waiter.
+  //   kraw_*, vraw_*        copy warps <-> dequantisation, per ring stage
+  //   k_full                K dequantisation -> MMA (also "Q is staged")
+  //   k_empty               MMA commit after S(j): K buffer kb free, S(j) done
+  //   v_full                V dequantisation -> MMA: V^T of tile j
   //   s_full / s_empty      S(j) in tensor memory / in the softmax registers
-  //   p_full / p_empty      P(j) in shared memory / O += P V of tile j done
+  //   p_full                softmax -> MMA: P(j) in shared memory
+  //   pv_done               MMA commit after O += P V of tile j: V^T and P free,
+  //                         O holds tiles .. j
   const uint32_t bars = base + SM::kBar;
-  const uint32_t raw_full = bars, raw_empty = raw_full + 8 * kStages;
-  const uint32_t k_full = raw_empty + 8 * kStages, k_empty = k_full + 8 * NB, v_full = k_empty + 8 * NB,
-                 v_empty = v_full + 8 * NB;
-  const uint32_t s_full = v_empty + 8 * NB, s_empty = s_full + 16, p_full = s_empty + 16, p_empty = p_full + 16,
-                 drain = p_empty + 16;
+  const uint32_t kraw_full = bars, kraw_empty = kraw_full + 8 * kKS, vraw_full = kraw_empty + 8 * kKS,
+                 vraw_empty = vraw_full + 8 * kVS;
+  const uint32_t k_full = vraw_empty + 8 * kVS, k_empty = k_full + 16, v_full = k_empty + 16, s_full = v_full + 8,
+                 s_empty = s_full + 16, p_full = s_empty + 16, pv_done = p_full + 8, drain = pv_done + 8;
   volatile int* abort = reinterpret_cast<volatile int*>(smem + SM::kMisc);
   int* start = reinterpret_cast<int*>(smem + SM::kMisc + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM::kMisc + 16);
-  const uint32_t ring = base + SM::kRing;
-  auto kbuf = [&](int kb) { return base + SM::kK0 + kb * SM::kKBuf; };
-  auto vbuf = [&](int kb) { return base + SM::kV0 + kb * SM::kVBytes; };
-  auto pbuf = [&](int sb) { return base + SM::kP0 + sb * SM::kPBytes; };
+  const uint32_t kring = base + SM::kRing, vring = base + SM::kVRing;
 
   const long long T = p.total_tiles;
   const int Gn = p.n_ctas;
@@ -290,22 +297,23 @@ __global__ void __launch_bounds__(kRowThreads, 1) pa_rows_tc_kernel(const __grid
   if (tid == 0) {
     asm volatile("griddepcontrol.launch_dependents;");
     *abort = 0;
-    for (int i = 0; i < kStages; ++i) {
-      mbar_init(raw_full + 8 * i, 1);
-      mbar_init(raw_empty + 8 * i, 8);  // four K and four V warps
+    for (int i = 0; i < kKS; ++i) {
+      mbar_init(kraw_full + 8 * i, 1);
+      mbar_init(kraw_empty + 8 * i, 4);
     }
-    for (int i = 0; i < NB; ++i) {
-      mbar_init(k_full + 8 * i, 4);
-      mbar_init(k_empty + 8 * i, 1);
-      mbar_init(v_full + 8 * i, 4);
-      mbar_init(v_empty + 8 * i, 1);
+    for (int i = 0; i < kVS; ++i) {
+      mbar_init(vraw_full + 8 * i, 1);
+      mbar_init(vraw_empty + 8 * i, 4);
     }
     for (int i = 0; i < 2; ++i) {
+      mbar_init(k_full + 8 * i, 4);
+      mbar_init(k_empty + 8 * i, 1);
       mbar_init(s_full + 8 * i, 1);
       mbar_init(s_empty + 8 * i, 4);
-      mbar_init(p_full + 8 * i, 4);
-      mbar_init(p_empty + 8 * i, 1);
     }
+    mbar_init(v_full, 4);
+    mbar_init(p_full, 4);
+    mbar_init(pv_done, 1);
     mbar_init(drain, 1);
     fence_mbar_init();
     const RowPos r = row_locate(p, a);
@@ -331,17 +339,21 @@ __global__ void __launch_bounds__(kRowThreads, 1) pa_rows_tc_kernel(const __grid
   const int R = kGqa * p.n_qtok;
   const int n = (int)(b - a);
 
-  if (any && w == kTcCopyWarp) {
-    // ---- raw K/V stages
+  if (any && (w == kTcCopyK || w == kTcCopyV)) {
+    // ---- raw K (or V) stages, two per key tile
+    const bool isv = w == kTcCopyV;
+    const int ns = isv ? kVS : kKS, sb = isv ? SM::kVStage : SM::kKStage;
+    const uint32_t full = isv ? vraw_full : kraw_full, empty = isv ? vraw_empty : kraw_empty, rg0 = isv ? vring : kring;
     const uint64_t policy = l2_evict_first_policy();
     RowPos pos = pos0;
-    for (int j = 0; j < n; ++j) {
+    for (int q = 0; q < 2 * n; ++q) {
       if (__any_sync(0xffffffffu, *abort != 0)) break;
-      const int slot = j % kStages, use = j / kStages;
-      if (use > 0) mbar_wait(raw_empty + 8 * slot, (use - 1) & 1, p.err, abort);
-      const int tb = row_entry(p, pos, lane);
-      issue_stage<KT, VT>(p, pos, tb, ring + slot * G::kBytes, raw_full + 8 * slot, policy, lane);
-      row_next(p, pos);
+      const int slot = q % ns, use = q / ns, half = q & 1;
+      if (use > 0) mbar_wait(empty + 8 * slot, (use - 1) & 1, p.err, abort);
+      const int tb = row_entry(p, pos, half, lane);
+      if (isv) issue_half<VT, true>(p, pos, half, tb, rg0 + slot * sb, full + 8 * slot, policy, lane);
+      else issue_half<KT, false>(p, pos, half, tb, rg0 + slot * sb, full + 8 * slot, policy, lane);
+      if (half) row_next(p, pos);
     }
   } else if (any && w >= kTcKWarp0 && w < kTcKWarp0 + 4) {
     // ---- K dequantisation, and Q into tensor memory at every piece start
@@ -349,107 +361,103 @@ __global__ void __launch_bounds__(kRowThreads, 1) pa_rows_tc_kernel(const __grid
     RowPos pos = pos0;
     for (int j = 0; j < n; ++j) {
       const TcTile tt = tc_tile(pos, a + j, a, b);
-      const int kb = j % NB, ku = j / NB, slot = j % kStages;
+      const int kb = j & 1, ku = j >> 1;
       if (tt.first) {
         if (j > 0) {  // S(j - 1), the previous piece's last, is done with Q
-          mbar_wait(k_empty + 8 * ((j - 1) % NB), ((j - 1) / NB) & 1, p.err, abort);
+          mbar_wait(k_empty + 8 * ((j - 1) & 1), ((j - 1) >> 1) & 1, p.err, abort);
           __syncwarp();
           tc_fence_after();
         }
         tc_stage_q<KT>(p, pos.s, pos.gi / p.n_row_tiles, pos.gi % p.n_row_tiles,
                        tmem + kTcQCol + ((uint32_t)(32 * dw) << 16), dw, lane);
       }
-      mbar_wait(raw_full + 8 * slot, (j / kStages) & 1, p.err, abort);
-      if (ku > 0) mbar_wait(k_empty + 8 * kb, (ku - 1) & 1, p.err, abort);  // S(j - 3) is done with the buffer
-      __syncwarp();
-      const int n_keys = min(kRowKeys, pos.L - pos.j * kRowKeys);
-      tc_dequant_warp<KT, false>(ring + slot * G::kBytes, kbuf(kb), kbuf(kb) + SM::kKBytes, dw, lane, n_keys);
+      if (ku > 0) mbar_wait(k_empty + 8 * kb, (ku - 1) & 1, p.err, abort);  // S(j - 2) is done with the buffer
+      const uint32_t kh = base + SM::kK0 + kb * SM::kKBuf;
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        const int q = 2 * j + half, slot = q % kKS;
+        mbar_wait(kraw_full + 8 * slot, (q / kKS) & 1, p.err, abort);
+        __syncwarp();
+        const int n_keys = min(kStageKeys, pos.L - pos.j * kRowKeys - half * kStageKeys);
+        const uint32_t off = (uint32_t)(half * kStageKeys * kD * 2);
+        tc_dequant_warp<KT, false>(kring + slot * SM::kKStage, kh + off, kh + SM::kKBytes + off, dw, 0, lane, n_keys);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(kraw_empty + 8 * slot);
+      }
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(raw_empty + 8 * slot);
-        mbar_arrive(k_full + 8 * kb);
-      }
+      if (lane == 0) mbar_arrive(k_full + 8 * kb);
       row_next(p, pos);
     }
   } else if (any && w >= kTcVWarp0 && w < kTcVWarp0 + 4) {
-    // ---- V dequantisation
+    // ---- V dequantisation into the single V^T buffer
     const int dw = w - kTcVWarp0;
     RowPos pos = pos0;
     for (int j = 0; j < n; ++j) {
-      const int kb = j % NB, ku = j / NB, slot = j % kStages;
-      mbar_wait(raw_full + 8 * slot, (j / kStages) & 1, p.err, abort);
-      if (ku > 0) mbar_wait(v_empty + 8 * kb, (ku - 1) & 1, p.err, abort);  // O += P V of tile j - 3 is done with it
-      __syncwarp();
-      const int n_keys = min(kRowKeys, pos.L - pos.j * kRowKeys);
-      tc_dequant_warp<VT, true>(ring + slot * G::kBytes + G::kKBytes, vbuf(kb), 0u, dw, lane, n_keys);
+      if (j > 0) mbar_wait(pv_done, (j - 1) & 1, p.err, abort);  // O += P V of tile j - 1 is done with it
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        const int q = 2 * j + half, slot = q % kVS;
+        mbar_wait(vraw_full + 8 * slot, (q / kVS) & 1, p.err, abort);
+        __syncwarp();
+        const int n_keys = min(kStageKeys, pos.L - pos.j * kRowKeys - half * kStageKeys);
+        tc_dequant_warp<VT, true>(vring + slot * SM::kVStage, base + SM::kV0, 0u, dw, half * (kStageKeys / 8) + dw, lane,
+                                  n_keys);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(vraw_empty + 8 * slot);
+      }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(raw_empty + 8 * slot);
-        mbar_arrive(v_full + 8 * kb);
-      }
+      if (lane == 0) mbar_arrive(v_full);
       row_next(p, pos);
     }
   } else if (any && w == kTcMmaWarp) {
     // ---- MMA issue (the whole warp, one elected lane issuing): S(j), then
     // O += P V of tile j - 1
     const uint32_t tq = __shfl_sync(0xffffffffu, tmem, 0), ub = __shfl_sync(0xffffffffu, base, 0);
-    const uint64_t kdesc0 = smem_desc(ub + SM::kK0, 128, 4096), vdesc0 = smem_desc(ub + SM::kV0, 128, 512),
-                   pdesc0 = smem_desc(ub + SM::kP0, 128, 512);
     // descriptor start addresses count 16-byte units
+    const uint64_t kdesc0 = smem_desc(ub + SM::kK0, 128, 4096), vdesc = smem_desc(ub + SM::kV0, 128, 1024),
+                   pdesc = smem_desc(ub + SM::kP0, 128, 1024);
     auto pv = [&](int jj, bool first) {
-      const int kb = jj % NB, sb = jj & 1;
-      mbar_wait(v_full + 8 * kb, (jj / NB) & 1, p.err, abort);
-      mbar_wait(p_full + 8 * sb, (jj >> 1) & 1, p.err, abort);
+      mbar_wait(v_full, jj & 1, p.err, abort);
+      mbar_wait(p_full, jj & 1, p.err, abort);
       __syncwarp();
       tc_fence_after();
-      const uint64_t pd = pdesc0 + (uint64_t)((sb * SM::kPBytes) >> 4), vd = vdesc0 + (uint64_t)((kb * SM::kVBytes) >> 4);
 #pragma unroll
       for (int kk = 0; kk < kRowKeys / 16; ++kk)
-        tc_mma_f16_warp(tq + kTcOCol, pd + 16 * kk, vd + 16 * kk, kTcIdescO, (first && kk == 0) ? 0u : 1u);
-      tc_commit_warp(v_empty + 8 * kb);
-      tc_commit_warp(p_empty + 8 * sb);
+        tc_mma_f16_warp(tq + kTcOCol, pdesc + 16 * kk, vdesc + 16 * kk, kTcIdescO, (first && kk == 0) ? 0u : 1u);
+      tc_commit_warp(pv_done);
     };
     RowPos pos = pos0;
     bool prev_first = false;
     for (int j = 0; j < n; ++j) {
-      const int kb = j % NB, sb = j & 1, su = j >> 1;
+      const int kb = j & 1, ku = j >> 1;
       const bool first = tc_tile(pos, a + j, a, b).first;
-      mbar_wait(k_full + 8 * kb, (j / NB) & 1, p.err, abort);
-      if (su > 0) mbar_wait(s_empty + 8 * sb, (su - 1) & 1, p.err, abort);
+      mbar_wait(k_full + 8 * kb, ku & 1, p.err, abort);
+      if (ku > 0) mbar_wait(s_empty + 8 * kb, (ku - 1) & 1, p.err, abort);
       __syncwarp();
       tc_fence_after();
-      // two chains: Q K_hi^T and Q K_lo^T, or (binary16 K) the two halves of the dims
-      const uint32_t dA = tq + kTcSCol + 2 * kRowKeys * sb, dB = dA + kRowKeys;
+      const uint32_t dS = tq + kTcSCol + kRowKeys * kb;
       const uint64_t kd = kdesc0 + (uint64_t)((kb * SM::kKBuf) >> 4);
+#pragma unroll
+      for (int ks = 0; ks < kD / 16; ++ks)
+        tc_mma_f16_tmem_a_warp(dS, tq + kTcQCol + 8 * ks, kd + 16 * ks, kTcIdescS, ks > 0);
       if (SM::kKSplit) {
 #pragma unroll
-        for (int ks = 0; ks < kD / 16; ++ks) {
-          tc_mma_f16_tmem_a_warp(dA, tq + kTcQCol + 8 * ks, kd + 16 * ks, kTcIdescS, ks > 0);
-          tc_mma_f16_tmem_a_warp(dB, tq + kTcQCol + 8 * ks, kd + (SM::kKBytes >> 4) + 16 * ks, kTcIdescS, ks > 0);
-        }
-      } else {
-#pragma unroll
-        for (int ks = 0; ks < kD / 32; ++ks) {
-          tc_mma_f16_tmem_a_warp(dA, tq + kTcQCol + 8 * ks, kd + 16 * ks, kTcIdescS, ks > 0);
-          tc_mma_f16_tmem_a_warp(dB, tq + kTcQCol + 8 * (ks + kD / 32), kd + 16 * (ks + kD / 32), kTcIdescS, ks > 0);
-        }
+        for (int ks = 0; ks < kD / 16; ++ks)
+          tc_mma_f16_tmem_a_warp(dS, tq + kTcQCol + 8 * ks, kd + (SM::kKBytes >> 4) + 16 * ks, kTcIdescS, 1);
       }
       tc_commit_warp(k_empty + 8 * kb);
-      tc_commit_warp(s_full + 8 * sb);
+      tc_commit_warp(s_full + 8 * kb);
       if (j > 0) pv(j - 1, prev_first);
       prev_first = first;
       row_next(p, pos);
     }
     if (n > 0) pv(n - 1, prev_first);
     // the last commits have arrived before the CTA's barriers go away
-    for (int jj = max(0, n - NB); jj < n; ++jj) {
-      mbar_wait(k_empty + 8 * (jj % NB), (jj / NB) & 1, p.err, abort);
-      mbar_wait(v_empty + 8 * (jj % NB), (jj / NB) & 1, p.err, abort);
-    }
-    for (int jj = max(0, n - 2); jj < n; ++jj) mbar_wait(p_empty + 8 * (jj & 1), (jj >> 1) & 1, p.err, abort);
+    for (int jj = max(0, n - 2); jj < n; ++jj) mbar_wait(k_empty + 8 * (jj & 1), (jj >> 1) & 1, p.err, abort);
+    if (n > 0) mbar_wait(pv_done, (n - 1) & 1, p.err, abort);
     __syncwarp();
   } else if (any && w < kTcSmWarp0 + 4) {
     // ---- softmax and output: one query row per thread
@@ -457,13 +465,14 @@ __global__ void __launch_bounds__(kRowThreads, 1) pa_rows_tc_kernel(const __grid
     const uint32_t t_lane = (uint32_t)(32 * w) << 16;
     const uint32_t tO = tmem + kTcOCol + t_lane;
     const float scale_log2 = p.scale_log2;
+    const uint32_t pk = base + SM::kP0;
     RowPos pos = pos0;
     float m = -INFINITY, l = 0.f;
     int vis = -1, piece_j0 = 0;
     bool piece_whole = false;
     for (int j = 0; j < n; ++j) {
       const TcTile tt = tc_tile(pos, a + j, a, b);
-      const int sb = j & 1, su = j >> 1;
+      const int kb = j & 1, ku = j >> 1;
       const int rt = pos.gi % p.n_row_tiles, rg = kRowTile * rt + row;
       const bool smx = kRowTile * rt + 32 * w < R;  // the warp holds a real row
       if (tt.first) {
@@ -474,39 +483,42 @@ __global__ void __launch_bounds__(kRowThreads, 1) pa_rows_tc_kernel(const __grid
         piece_whole = pos.j == 0;
       }
       const int k0 = pos.j * kRowKeys;
-      // S(j) (the sum of its two partials) into registers; the buffer is then
-      // free for S(j + 2)
-      mbar_wait(s_full + 8 * sb, su & 1, p.err, abort);
+      // S(j) into registers; the buffer is then free for S(j + 2)
+      mbar_wait(s_full + 8 * kb, ku & 1, p.err, abort);
       __syncwarp();
       tc_fence_after();
-      uint32_t sa[32], sv[32];
-      tmem_ld32(tmem + t_lane + kTcSCol + 2 * kRowKeys * sb, sa);
-      tmem_ld32(tmem + t_lane + kTcSCol + 2 * kRowKeys * sb + kRowKeys, sv);
+      uint32_t sv[64];
+      tmem_ld32(tmem + t_lane + kTcSCol + kRowKeys * kb, *reinterpret_cast<uint32_t(*)[32]>(sv));
+      tmem_ld32(tmem + t_lane + kTcSCol + kRowKeys * kb + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(s_empty + 8 * sb);
-      float x[32];
-#pragma unroll
-      for (int c = 0; c < kRowKeys; ++c) x[c] = __uint_as_float(sa[c]) + __uint_as_float(sv[c]);
+      if (lane == 0) mbar_arrive(s_empty + 8 * kb);
       if (k0 + kRowKeys - 1 > vis) {  // the causal edge (or padding rows): mask
 #pragma unroll
         for (int c = 0; c < kRowKeys; ++c)
-          if (k0 + c > vis) x[c] = -INFINITY;
+          if (k0 + c > vis) sv[c] = __float_as_uint(-INFINITY);
       }
       float mx[8];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) mx[c] = fmaxf(fmaxf(x[c], x[c + 8]), fmaxf(x[c + 16], x[c + 24]));
-      const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) *
-                         scale_log2;
+      for (int c = 0; c < 8; ++c)
+        mx[c] = fmaxf(fmaxf(fmaxf(__uint_as_float(sv[c]), __uint_as_float(sv[c + 8])),
+                            fmaxf(__uint_as_float(sv[c + 16]), __uint_as_float(sv[c + 24]))),
+                      fmaxf(fmaxf(__uint_as_float(sv[c + 32]), __uint_as_float(sv[c + 40])),
+                            fmaxf(__uint_as_float(sv[c + 48]), __uint_as_float(sv[c + 56]))));
+      const float tmax =
+          fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) *
+          scale_log2;
       // Lazy maximum: raised (rarely, after a row's first tile) past 2^8.  The
       // row of O is rescaled in tensor memory once O += P V of tile j - 1 is
       // done; tensor-memory loads and stores are warp-wide, so the whole warp
       // runs them when any of its rows rises.
       const bool raise = tmax > m + kLazy;
       const float al = raise ? ((m == -INFINITY) ? 1.f : ex2(m - tmax)) : 1.f;
+      // O += P V of tile j - 1 has read the P buffer (and, within a piece, O
+      // holds it) before P(j) is written or O rescaled
+      if (j > 0) mbar_wait(pv_done, (j - 1) & 1, p.err, abort);
       if (smx && __any_sync(0xffffffffu, raise) && j > piece_j0) {
-        mbar_wait(p_empty + 8 * ((j - 1) & 1), ((j - 1) >> 1) & 1, p.err, abort);
         __syncwarp();
         tc_fence_after();
 #pragma unroll 1
@@ -519,31 +531,32 @@ __global__ void __launch_bounds__(kRowThreads, 1) pa_rows_tc_kernel(const __grid
           tmem_st32(tO + c, ov);
         }
         tmem_st_wait();
+        tc_fence_before();
       }
       if (raise) {
         l *= al;
         m = tmax;
       }
       const float nbm = (m == -INFINITY) ? 0.f : -m;
-      uint32_t ph[16];
       float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const float e0 = ex2(fmaf(x[2 * c], scale_log2, nbm)), e1 = ex2(fmaf(x[2 * c + 1], scale_log2, nbm));
-        ls[c & 3] += e0 + e1;
-        ph[c] = pack_half2(e0, e1);
+      for (int kc = 0; kc < kRowKeys / 8; ++kc) {
+        uint32_t ph[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int c = 8 * kc + 2 * e;
+          const float e0 = ex2(fmaf(__uint_as_float(sv[c]), scale_log2, nbm)),
+                      e1 = ex2(fmaf(__uint_as_float(sv[c + 1]), scale_log2, nbm));
+          ls[e] += e0 + e1;
+          ph[e] = pack_half2(e0, e1);
+        }
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(pk + canon_off(row, kc, kRowKeys / 8)),
+                     "r"(ph[0]), "r"(ph[1]), "r"(ph[2]), "r"(ph[3]) : "memory");
       }
       l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-      // P(j) into shared-memory buffer sb once O += P V of tile j - 2 has read it
-      if (su > 0) mbar_wait(p_empty + 8 * sb, (su - 1) & 1, p.err, abort);
-      const uint32_t pk = pbuf(sb);
-#pragma unroll
-      for (int kc = 0; kc < kRowKeys / 8; ++kc)
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(pk + canon_off(row, kc, kRowKeys / 8)),
-                     "r"(ph[4 * kc]), "r"(ph[4 * kc + 1]), "r"(ph[4 * kc + 2]), "r"(ph[4 * kc + 3]) : "memory");
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full + 8 * sb);
+      if (lane == 0) mbar_arrive(p_full);
 
       if (tt.last && smx) {
         // ---- piece result: this thread's row, once the piece's last O += P V is done
@@ -551,7 +564,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) pa_rows_tc_kernel(const __grid
         const bool whole = piece_whole && pos.j + 1 == pos.nt;
         const bool len_ok = device_len(p, s) == pos.L;
         if (!len_ok && lane == 0) record_error(p.err, PA_ERR_BOUNDS);
-        mbar_wait(p_empty + 8 * sb, su & 1, p.err, abort);
+        mbar_wait(pv_done, j & 1, p.err, abort);
         __syncwarp();
         tc_fence_after();
         const bool real = rg < R;
@@ -595,9 +608,11 @@ __global__ void __launch_bounds__(kRowThreads, 1) pa_rows_tc_kernel(const __grid
     tc_commit_warp(drain);
     mbar_wait(drain, 0, p.err, abort, /*honour_abort=*/false);
   }
-  if (*abort && w == kTcCopyWarp && lane == 0) {
-    for (int k = n > kStages ? n - kStages : 0; k < n; ++k)
-      mbar_wait(raw_full + 8 * (k % kStages), (uint32_t)((k / kStages) & 1), p.err, abort, false, kWaitTimeoutNs / 8);
+  if (*abort && (w == kTcCopyK || w == kTcCopyV) && lane == 0) {
+    const int ns = w == kTcCopyV ? kVS : kKS;
+    const uint32_t full = w == kTcCopyV ? vraw_full : kraw_full;
+    for (int k = 2 * n > ns ? 2 * n - ns : 0; k < 2 * n; ++k)
+      mbar_wait(full + 8 * (k % ns), (uint32_t)((k / ns) & 1), p.err, abort, false, kWaitTimeoutNs / 8);
   }
   tc_fence_before();
   __syncthreads();

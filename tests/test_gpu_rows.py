@@ -99,7 +99,7 @@ def test_row_tiles_paged_equals_contiguous_and_repeats():
 
 
 def test_row_tiles_plan():
-    """A row tile takes the 32-key tiles its last row sees: earlier row tiles
+    """A row tile takes the 64-key tiles its last row sees: earlier row tiles
     of a long verify batch stop short of the newest keys."""
     w = W.make_workload("rows-plan", 82, [5000, 300], 16, Q8, Q8, 96, "shuffled")
     c, _ = device_cache(w)
@@ -108,8 +108,8 @@ def test_row_tiles_plan():
     for L in w.seq_lens:
         for rt in range(5):  # 576 rows = five row tiles of 128
             t_last = min(95, (128 * (rt + 1) - 1) // 6)
-            tiles += (int(L) - 96 + t_last + 1 + 31) // 32
-    assert plan["tiles"] == tiles * W.HKV and plan["tile_keys"] == 32
+            tiles += (int(L) - 96 + t_last + 1 + 63) // 64
+    assert plan["tiles"] == tiles * W.HKV and plan["tile_keys"] == 64
 
 
 def test_row_tiles_sub_batches():
