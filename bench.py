@@ -51,7 +51,8 @@ PAGES_PAGED_3090_MS = 4.095
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
 DECODE_SOURCES = ["paged_kv_gqa_11_gb300/csrc/pa_decode.cu", "paged_kv_gqa_11_gb300/csrc/pa_decode_impl.cuh",
                   "paged_kv_gqa_11_gb300/csrc/pa_decode_kern.cu", "paged_kv_gqa_11_gb300/csrc/pa_device.cuh",
-                  "paged_kv_gqa_11_gb300/csrc/pa_layout.cuh", "paged_kv_gqa_11_gb300/csrc/pa_rows_impl.cuh"]
+                  "paged_kv_gqa_11_gb300/csrc/pa_layout.cuh", "paged_kv_gqa_11_gb300/csrc/pa_rows_impl.cuh",
+                  "paged_kv_gqa_11_gb300/csrc/pa_rows_tc.cuh"]
 
 
 def workload_for(name: str) -> W.Workload:
