@@ -221,11 +221,8 @@ bool lookup_rows_tc_kernel(int kt, int vt, KernelInfo* out) {
 }
 
 // Query tokens from which the row-tile kernel takes over from the decode
-// kernels.
-#ifndef PA_ROWS_FROM
-#define PA_ROWS_FROM 9
-#endif
-constexpr uint32_t kRowsFromQTok = PA_ROWS_FROM;
+// kernels (measured: the decode kernels are faster up to eight tokens).
+constexpr uint32_t kRowsFromQTok = 9;
 
 // The split kernel for n_qtok query tokens: the decode kernels below
 // kRowsFromQTok tokens (by n-tiles of 8 query rows), the row-tile kernel from
@@ -290,7 +287,7 @@ pa_status check_shape(const pa_pool* pool, uint32_t n_qtok, uint32_t n_q_heads, 
 // (16 keys of up to four KV heads; the group is the largest of 4, 3, 2, 1 that
 // divides the KV head count), two to eight tokens per-head tiles of 64 keys,
 // and nine to 96 tokens row tiles (segments of 128 query rows of one KV head,
-// 32-key tiles).
+// 64-key tiles).
 struct Geometry {
   int tile_keys, seg_heads, segs_per_seq, rows_per_seg;
   int n_row_tiles;  // row tiles per KV head, or 0
