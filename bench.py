@@ -692,7 +692,7 @@ def main():
             "split_us": round(split * 1e3, 2),
         } if not tensor_bound else {
             "bound": "tensor",
-            "kernel": "pa_rows_decode_kernel",
+            "kernel": "pa_rows_tc_kernel",
             "achieved": round(flops / (split * 1e-3) / 1e12, 2),
             "peak": tpeak,
             "unit": "TFLOP/s",
