@@ -1276,8 +1276,10 @@ __device__ void consume_shared(const DecodeParams& p, uint8_t* smem, uint32_t ri
           for (int e = 0; e < 2; ++e) l_part[nt][e] += rs[nt][e];
       }
 
-      // ---- PV phase: dims of m-tiles 4*warp .. +3 over all 64 keys
-#pragma unroll
+      // ---- PV phase: dims of m-tiles 4*warp .. +3 over all 64 keys (from three
+      // n-tiles on, unrolled by two only: the fully unrolled loop no longer
+      // fits the instruction cache)
+#pragma unroll(NT >= 3 ? 2 : kCWarps)
       for (int kw = 0; kw < kCWarps; ++kw) {
         uint32_t bp[NT][2];
 #pragma unroll

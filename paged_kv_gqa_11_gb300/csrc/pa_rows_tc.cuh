@@ -163,7 +163,7 @@ __device__ __forceinline__ void tc_dequant_warp(uint32_t region, uint32_t dst, u
     asm volatile("ld.shared.u16 %0, [%1];" : "=h"(dh) : "r"(sgrp + off));
     return live ? ((uint32_t)dh | ((uint32_t)dh << 16)) : 0u;  // a zero scale zeroes the key
   };
-#pragma unroll
+#pragma unroll 1  // rolled: fifteen warps run different code, and the instruction cache is the limit
   for (int i = 0; i < C / 4; ++i) {
     uint32_t x[4];  // chunk 4i + j of key g, bytes 4t .. 4t+3 (thread 4g + t)
     ldsm_x4(lrow + (((4 * i + (lane >> 3)) ^ (lr & 7)) << 4), x);
