@@ -440,11 +440,11 @@ __global__ void __launch_bounds__(kRowThreads, 1) pa_rows_tc_kernel(const __grid
       tc_fence_after();
       const uint32_t dS = tq + kTcSCol + kRowKeys * kb;
       const uint64_t kd = kdesc0 + (uint64_t)((kb * SM::kKBuf) >> 4);
-#pragma unroll
+#pragma unroll 4
       for (int ks = 0; ks < kD / 16; ++ks)
         tc_mma_f16_tmem_a_warp(dS, tq + kTcQCol + 8 * ks, kd + 16 * ks, kTcIdescS, ks > 0);
       if (SM::kKSplit) {
-#pragma unroll
+#pragma unroll 4
         for (int ks = 0; ks < kD / 16; ++ks)
           tc_mma_f16_tmem_a_warp(dS, tq + kTcQCol + 8 * ks, kd + (SM::kKBytes >> 4) + 16 * ks, kTcIdescS, 1);
       }
@@ -495,9 +495,9 @@ __global__ void __launch_bounds__(kRowThreads, 1) pa_rows_tc_kernel(const __grid
       __syncwarp();
       if (lane == 0) mbar_arrive(s_empty + 8 * kb);
       if (k0 + kRowKeys - 1 > vis) {  // the causal edge (or padding rows): mask
+        const int nv = vis - k0 + 1;  // keys of this tile the row sees (may be <= 0)
 #pragma unroll
-        for (int c = 0; c < kRowKeys; ++c)
-          if (k0 + c > vis) sv[c] = __float_as_uint(-INFINITY);
+        for (int c = 0; c < kRowKeys; ++c) sv[c] = c < nv ? sv[c] : 0xff800000u;  // -inf
       }
       float mx[8];
 #pragma unroll
