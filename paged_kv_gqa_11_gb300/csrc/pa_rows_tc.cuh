@@ -34,9 +34,10 @@
 //   warps 4-7   K dequantisation, sixteen keys each per tile, into one of two
 //               binary16 K buffers; Q into tensor memory at a segment start;
 //   warps 8-11  V dequantisation into the V^T buffer, sixteen keys each;
-//   warp 12     issues the MMAs (one thread): S of tile j + 1 goes to the
-//               tensor core before O += P V of tile j, so S is computed while
-//               the softmax of tile j runs;
+//   warp 12     issues the MMAs (the whole warp runs the loop on warp-uniform
+//               descriptors; one lane, chosen by elect.sync, issues): S of tile
+//               j + 1 goes to the tensor core before O += P V of tile j, so S is
+//               computed while the softmax of tile j runs;
 //   warps 13-14 stream raw K (warp 13) and V (warp 14) row groups into two
 //               rings of 32-key stages (bulk copies), two stages per key
 //               tile; separate rings let K run ahead of V, which waits for
@@ -66,7 +67,7 @@ namespace pa_split {
 
 constexpr uint32_t kTcTmemCols = 512;
 constexpr uint32_t kTcOCol = 0, kTcQCol = 256, kTcSCol = 384;  // O, Q, S[2] (64 columns each)
-constexpr uint32_t kTcIdescS = idesc_f16_f32(kRowTile, kRowKeys);  // 128 x 32
+constexpr uint32_t kTcIdescS = idesc_f16_f32(kRowTile, kRowKeys);  // 128 x 64
 constexpr uint32_t kTcIdescO = idesc_f16_f32(kRowTile, kD);        // 128 x 256
 constexpr int kTcSmWarp0 = 0, kTcKWarp0 = 4, kTcVWarp0 = 8, kTcMmaWarp = 12, kTcCopyK = 13, kTcCopyV = 14;
 constexpr int kRowThreads = 15 * 32;
