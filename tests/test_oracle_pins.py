@@ -277,7 +277,9 @@ def pin_dense_brute_force():
     cases = [([7, 1, 20], 16, W.TYPE_F16, W.TYPE_F16, 1),
              ([33, 16], 16, W.TYPE_Q4_0, W.TYPE_Q4_0, 2),
              ([5, 40], 32, W.TYPE_Q8_0, W.TYPE_Q8_0, 4),
-             ([18, 50], 48, W.TYPE_Q8_0, W.TYPE_Q4_0, 3)]
+             ([18, 50], 48, W.TYPE_Q8_0, W.TYPE_Q4_0, 3),
+             ([20, 37], 16, W.TYPE_Q8_0, W.TYPE_Q4_0, 20),   # row-tile widths, L = n_qtok included
+             ([96, 130], 16, W.TYPE_F16, W.TYPE_Q8_0, 96)]
     for i, (lens, ps, kt, vt, nq) in enumerate(cases):
         w = W.make_workload("bf", 100 + i, lens, ps, kt, vt, nq, "shuffled")
         out, lse = oracle.decode_workload(w)
