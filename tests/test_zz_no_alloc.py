@@ -34,6 +34,8 @@ CASES = {
     "q8-4tok": ([9000, 777, 130], 256, W.TYPE_Q8_0, 4),
     # more sequences than one launch takes: sub-batches through the one array
     "q8-3tok-300seq": ([40 + (37 * i) % 500 for i in range(300)], 16, W.TYPE_Q8_0, 3),
+    # row tiles (tcgen05 kernel), two row tiles per KV head, a sequence with L = n_qtok
+    "q8-40tok": ([3000, 40, 700], 16, W.TYPE_Q8_0, 40),
 }
 
 
@@ -58,7 +60,7 @@ def _both(name):
 
 
 def test_noalloc_is_bit_identical_over_calls_of_different_shapes():
-    for call, name in enumerate(["q4-1tok", "q8-4tok", "q8-3tok-300seq", "q4-1tok"]):
+    for call, name in enumerate(["q4-1tok", "q8-4tok", "q8-40tok", "q8-3tok-300seq", "q4-1tok", "q8-40tok"]):
         (ro, rl), (go, gl) = _both(name)
         assert np.isfinite(go).all(), f"call {call} ({name})"
         assert np.array_equal(go, ro), f"call {call} ({name}): out differs from pa_decode"
