@@ -70,14 +70,14 @@ def test_noalloc_is_bit_identical_over_calls_of_different_shapes():
 def test_noalloc_refuses_batches_beyond_the_scratch():
     """A call whose scratch would exceed the array is refused on the host,
     before any launch (the pointers are never used).  One launch takes at most
-    128 sequences, so the scratch a call needs is bounded; on a device where
-    every shape fits, nothing is refused."""
+    128 sequences, so the scratch a call needs is bounded; the row tiles' 128
+    partial rows per segment take it past the array at 96 query tokens."""
     p = pa.Pool(64, 16, 4, 256, pa.PA_Q4_0)
     dev = torch.cuda.current_device()
     n_seq = 100000
-    sl = np.full(n_seq, 16, np.int32)
     refused = 0
-    for nq in range(1, 9):
+    for nq in list(range(1, 9)) + [20, 96]:  # decode kernels and row tiles
+        sl = np.full(n_seq, max(16, nq), np.int32)
         need = pa.pa_decode_workspace_size(p, n_seq, nq, dev)
         assert need > 0
         if need > pa.NOALLOC_SCRATCH_BYTES:
