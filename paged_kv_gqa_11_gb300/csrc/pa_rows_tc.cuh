@@ -93,9 +93,10 @@ struct TcSmem {
   static_assert(kRing % 1024 == 0, "tile alignment");
   static constexpr int kVRing = kRing + kKStages * kKStage;
   // mbarriers: K raw full / empty [kKStages], V raw full / empty [kVStages],
-  // k full / empty [2], v full, s full / empty [2], p full, pv done, drain
+  // k full / empty [2], v full [2], s full / empty [2], p full, pv done [2],
+  // drain
   static constexpr int kBar = kVRing + kVStages * kVStage;
-  static constexpr int kNBar = 2 * kKStages + 2 * kVStages + 4 + 1 + 4 + 1 + 1 + 1;
+  static constexpr int kNBar = 2 * kKStages + 2 * kVStages + 4 + 2 + 4 + 1 + 2 + 1;
   static constexpr int kMisc = kBar + kNBar * 8;  // abort, start[3], tmem base
   static constexpr int kTotal = kMisc + 32;
   static constexpr int kLaunch = kTotal + 1024;  // the base is aligned to 1024 inside
@@ -276,16 +277,18 @@ __global__ void __launch_bounds__(kRowThreads, 1) pa_rows_tc_kernel(const __grid
   //   kraw_*, vraw_*        copy warps <-> dequantisation, per ring stage
   //   k_full                K dequantisation -> MMA (also "Q is staged")
   //   k_empty               MMA commit after S(j): K buffer kb free, S(j) done
-  //   v_full                V dequantisation -> MMA: V^T of tile j
+  //   v_full[h]             V dequantisation -> MMA: keys 32h .. 32h+31 of V^T
+  //                         (tile half h) of tile j
   //   s_full / s_empty      S(j) in tensor memory / in the softmax registers
   //   p_full                softmax -> MMA: P(j) in shared memory
-  //   pv_done               MMA commit after O += P V of tile j: V^T and P free,
+  //   pv_done[h]            MMA commit after O += P V of tile j's half h: that
+  //                         half of V^T free; pv_done[1] also: P free,
   //                         O holds tiles .. j
   const uint32_t bars = base + SM::kBar;
   const uint32_t kraw_full = bars, kraw_empty = kraw_full + 8 * kKS, vraw_full = kraw_empty + 8 * kKS,
                  vraw_empty = vraw_full + 8 * kVS;
-  const uint32_t k_full = vraw_empty + 8 * kVS, k_empty = k_full + 16, v_full = k_empty + 16, s_full = v_full + 8,
-                 s_empty = s_full + 16, p_full = s_empty + 16, pv_done = p_full + 8, drain = pv_done + 8;
+  const uint32_t k_full = vraw_empty + 8 * kVS, k_empty = k_full + 16, v_full = k_empty + 16, s_full = v_full + 16,
+                 s_empty = s_full + 16, p_full = s_empty + 16, pv_done = p_full + 8, drain = pv_done + 16;
   volatile int* abort = reinterpret_cast<volatile int*>(smem + SM::kMisc);
   int* start = reinterpret_cast<int*>(smem + SM::kMisc + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM::kMisc + 16);
@@ -313,8 +316,10 @@ __global__ void __launch_bounds__(kRowThreads, 1) pa_rows_tc_kernel(const __grid
       mbar_init(s_empty + 8 * i, 4);
     }
     mbar_init(v_full, 4);
+    mbar_init(v_full + 8, 4);
     mbar_init(p_full, 4);
     mbar_init(pv_done, 1);
+    mbar_init(pv_done + 8, 1);
     mbar_init(drain, 1);
     fence_mbar_init();
     const RowPos r = row_locate(p, a);
@@ -392,25 +397,28 @@ __global__ void __launch_bounds__(kRowThreads, 1) pa_rows_tc_kernel(const __grid
       row_next(p, pos);
     }
   } else if (any && w >= kTcVWarp0 && w < kTcVWarp0 + 4) {
-    // ---- V dequantisation into the single V^T buffer
+    // ---- V dequantisation into the single V^T buffer, half a tile at a time:
+    // half h of tile j is written once O += P V of tile j - 1 has read that
+    // half, so the conversion of one half overlaps the product of the other
     const int dw = w - kTcVWarp0;
     RowPos pos = pos0;
     for (int j = 0; j < n; ++j) {
-      if (j > 0) mbar_wait(pv_done, (j - 1) & 1, p.err, abort);  // O += P V of tile j - 1 is done with it
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {
         const int q = 2 * j + half, slot = q % kVS;
+        if (j > 0) mbar_wait(pv_done + 8 * half, (j - 1) & 1, p.err, abort);
         mbar_wait(vraw_full + 8 * slot, (q / kVS) & 1, p.err, abort);
         __syncwarp();
         const int n_keys = min(kStageKeys, pos.L - pos.j * kRowKeys - half * kStageKeys);
         tc_dequant_warp<VT, true>(vring + slot * SM::kVStage, base + SM::kV0, 0u, dw, half * (kStageKeys / 8) + dw, lane,
                                   n_keys);
+        fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(vraw_empty + 8 * slot);
+        if (lane == 0) {
+          mbar_arrive(vraw_empty + 8 * slot);
+          mbar_arrive(v_full + 8 * half);
+        }
       }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(v_full);
       row_next(p, pos);
     }
   } else if (any && w == kTcMmaWarp) {
@@ -420,15 +428,18 @@ __global__ void __launch_bounds__(kRowThreads, 1) pa_rows_tc_kernel(const __grid
     // descriptor start addresses count 16-byte units
     const uint64_t kdesc0 = smem_desc(ub + SM::kK0, 128, 4096), vdesc = smem_desc(ub + SM::kV0, 128, 1024),
                    pdesc = smem_desc(ub + SM::kP0, 128, 1024);
-    auto pv = [&](int jj, bool first) {
-      mbar_wait(v_full, jj & 1, p.err, abort);
+    auto pv = [&](int jj, bool first) {  // by tile halves, each as soon as its V^T is there
       mbar_wait(p_full, jj & 1, p.err, abort);
-      __syncwarp();
-      tc_fence_after();
 #pragma unroll
-      for (int kk = 0; kk < kRowKeys / 16; ++kk)
-        tc_mma_f16_warp(tq + kTcOCol, pdesc + 16 * kk, vdesc + 16 * kk, kTcIdescO, (first && kk == 0) ? 0u : 1u);
-      tc_commit_warp(pv_done);
+      for (int half = 0; half < 2; ++half) {
+        mbar_wait(v_full + 8 * half, jj & 1, p.err, abort);
+        __syncwarp();
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 2 * half; kk < 2 * half + 2; ++kk)
+          tc_mma_f16_warp(tq + kTcOCol, pdesc + 16 * kk, vdesc + 16 * kk, kTcIdescO, (first && kk == 0) ? 0u : 1u);
+        tc_commit_warp(pv_done + 8 * half);
+      }
     };
     RowPos pos = pos0;
     bool prev_first = false;
@@ -458,7 +469,10 @@ __global__ void __launch_bounds__(kRowThreads, 1) pa_rows_tc_kernel(const __grid
     if (n > 0) pv(n - 1, prev_first);
     // the last commits have arrived before the CTA's barriers go away
     for (int jj = max(0, n - 2); jj < n; ++jj) mbar_wait(k_empty + 8 * (jj & 1), (jj >> 1) & 1, p.err, abort);
-    if (n > 0) mbar_wait(pv_done, (n - 1) & 1, p.err, abort);
+    if (n > 0) {
+      mbar_wait(pv_done, (n - 1) & 1, p.err, abort);
+      mbar_wait(pv_done + 8, (n - 1) & 1, p.err, abort);
+    }
     __syncwarp();
   } else if (any && w < kTcSmWarp0 + 4) {
     // ---- softmax and output: one query row per thread
@@ -518,7 +532,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) pa_rows_tc_kernel(const __grid
       const float al = raise ? ((m == -INFINITY) ? 1.f : ex2(m - tmax)) : 1.f;
       // O += P V of tile j - 1 has read the P buffer (and, within a piece, O
       // holds it) before P(j) is written or O rescaled
-      if (j > 0) mbar_wait(pv_done, (j - 1) & 1, p.err, abort);
+      if (j > 0) mbar_wait(pv_done + 8, (j - 1) & 1, p.err, abort);
       if (smx && __any_sync(0xffffffffu, raise) && j > piece_j0) {
         __syncwarp();
         tc_fence_after();
@@ -565,7 +579,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) pa_rows_tc_kernel(const __grid
         const bool whole = piece_whole && pos.j + 1 == pos.nt;
         const bool len_ok = device_len(p, s) == pos.L;
         if (!len_ok && lane == 0) record_error(p.err, PA_ERR_BOUNDS);
-        mbar_wait(pv_done, j & 1, p.err, abort);
+        mbar_wait(pv_done + 8, j & 1, p.err, abort);
         __syncwarp();
         tc_fence_after();
         const bool real = rg < R;
