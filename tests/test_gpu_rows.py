@@ -139,6 +139,24 @@ def test_row_tiles_device_lengths_are_checked():
     assert cache.check() == PA_OK
 
 
+def test_row_tiles_bounds_guard_reports_and_stays_finite():
+    """A table entry outside the pool is never dereferenced: its rows read as
+    zeros, PA_ERR_BOUNDS is reported, the output stays finite and a sequence
+    that does not use the entry is unaffected (lucebox PR #555, Validation)."""
+    w = W.make_workload("rows-bnd", 85, [700, 90, 1500], 16, Q8, Q4, 20, "shuffled")
+    cache, _ = device_cache(w)
+    bad = w.table.copy()
+    bad[0, 5] = w.n_blocks + 1000
+    bad[2, 40] = -7
+    out, lse = cache.decode(to_dev(w.q), to_dev(bad), to_dev(w.seq_lens), w.seq_lens, 20, w.scale)
+    torch.cuda.synchronize()
+    assert cache.check() == PA_ERR_BOUNDS
+    assert torch.isfinite(out).all() and torch.isfinite(lse).all()
+    oo, ol = oracle.decode_workload(w)
+    assert_close(out.cpu().numpy()[1], oo[1], what="unaffected sequence")
+    assert_lse_close(lse.cpu().numpy()[1], ol[1], what="unaffected sequence")
+
+
 @pytest.mark.parametrize("ctx,nq", [(4096, 17), (16384, 65), (4096, 96)])
 def test_row_tile_workloads_sampled(ctx, nq):
     """The bench's row-tile workloads (one sequence, Q8_0 K / Q4_0 V): every
