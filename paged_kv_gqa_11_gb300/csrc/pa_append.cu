@@ -158,27 +158,41 @@ __global__ void __launch_bounds__(256) pa_append_kernel(const __grid_constant__ 
   const long long k_total = p.n_rows * p.n_kv_heads * p.k_units;
   const long long v_total = p.n_rows * p.n_kv_heads * p.v_units;
   const long long stride = (long long)gridDim.x * blockDim.x;
+  // Index arithmetic in 32 bits when the launch's units fit (the common case:
+  // a 64-bit division costs several times a 32-bit one, per unit).
+  const bool narrow = k_total + v_total <= 0xffffffffll;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < k_total + v_total; i += stride) {
     const bool is_k = i < k_total;
     const long long li = is_k ? i : i - k_total;
     const int units = is_k ? p.k_units : p.v_units;
-    const long long rh = li / units;  // (row, head)
-    const int u = (int)(li - rh * units);
-    const long long r = rh / p.n_kv_heads;
-    const int h = (int)(rh - r * p.n_kv_heads);
+    long long rh, r;  // (row, head), row
+    int u, h;
+    if (narrow) {
+      const uint32_t l = (uint32_t)li, rh32 = l / (uint32_t)units, r32 = rh32 / (uint32_t)p.n_kv_heads;
+      u = (int)(l - rh32 * (uint32_t)units);
+      h = (int)(rh32 - r32 * (uint32_t)p.n_kv_heads);
+      rh = rh32;
+      r = r32;
+    } else {
+      rh = li / units;
+      u = (int)(li - rh * units);
+      r = rh / p.n_kv_heads;
+      h = (int)(rh - r * p.n_kv_heads);
+    }
     const int s = __ldg(p.row_seq + r);
     const int pos = __ldg(p.row_pos + r);
-    if (s < 0 || s >= p.n_seq || pos < 0 || pos / p.page_size >= p.table_stride) {
+    if (s < 0 || s >= p.n_seq || pos < 0 || (uint32_t)pos / (uint32_t)p.page_size >= (uint32_t)p.table_stride) {
       if (u == 0 && h == 0 && is_k) record_error(p.err, PA_ERR_BOUNDS);
       continue;
     }
-    const int blk = __ldg(p.table + (long long)s * p.table_stride + pos / p.page_size);
+    const uint32_t page = (uint32_t)pos / (uint32_t)p.page_size;
+    const int blk = __ldg(p.table + (long long)s * p.table_stride + page);
     if (blk < 0 || blk >= p.n_blocks) {
       if (u == 0 && h == 0 && is_k) record_error(p.err, PA_ERR_BOUNDS);
       continue;
     }
     const int rb = is_k ? p.k_row : p.v_row;
-    const int slot = pos % p.page_size;
+    const int slot = (int)((uint32_t)pos - page * (uint32_t)p.page_size);
     const long long grp_row = ((long long)blk * p.n_kv_heads + h) * p.page_size + (slot & ~(kGroup - 1));
     uint8_t* grp = (is_k ? p.k_pool : p.v_pool) + grp_row * rb;
     if constexpr (kF16In) {
