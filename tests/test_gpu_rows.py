@@ -52,6 +52,7 @@ SMALL = [
     ("q4k-f16v-22-ps48", [130, 129], 48, Q4, F16, 22),
     ("q8-96-one-row-tile-edge", [150, 96], 16, Q8, Q8, 21),  # 126 rows: one row tile, 2 padding rows
     ("q8-43-two-row-tiles", [3000, 43], 16, Q8, Q8, 43),     # 258 rows: three row tiles, the last two rows
+    ("q4k-q8v-64-full-tiles", [200, 64, 1100], 32, Q4, Q8, 64),  # 384 rows: three full row tiles, no padding
 ]
 
 
