@@ -545,6 +545,63 @@ __device__ void produce_head(const DecodeParams& p, uint32_t ring, uint32_t bar_
 // ((kp * NT + nt) * 32 + lane) * 16, so one 16-byte load feeds a block's two
 // MMAs.
 
+// One Q fragment entry: what lane (g, t) holds of k-steps 2kp and 2kp+1 as
+// S-MMA B fragments (query row g), in the K format's dim order (kdim).  Quantised K:
+// v0 = dims 32 kp + 4t .. +3 (the block's low half), v1 = the same + 16 (its
+// high half, met as Q/16 by Q4_0's high nibbles); the entry is {(v0.x, v0.z),
+// (v0.y, v0.w), (v1.x, v1.z), (v1.y, v1.w)} in binary16, and lo / hi return
+// the fp32 sums, in dim order, of each half's binary16 values (the block bias
+// terms).  F16 K: v0 = dims 32 kp + 2t, +1, +8, +9 and v1 the same + 16, in
+// order.
+template <int KT>
+__device__ __forceinline__ uint4 q_entry(float4 v0, float4 v1, float& lo, float& hi) {
+  if constexpr (KT == PA_F16) {
+    lo = hi = 0.f;
+    return make_uint4(pack_half2(v0.x, v0.y), pack_half2(v0.z, v0.w), pack_half2(v1.x, v1.y),
+                      pack_half2(v1.z, v1.w));
+  } else {
+    constexpr float sc = KT == PA_Q4_0 ? 0.0625f : 1.f;
+    const uint32_t b0 = pack_half2(v0.x, v0.z), b1 = pack_half2(v0.y, v0.w);
+    const uint32_t b2 = pack_half2(sc * v1.x, sc * v1.z), b3 = pack_half2(sc * v1.y, sc * v1.w);
+    const float2 f0 = half2_bits_to_float2(b0), f1 = half2_bits_to_float2(b1);
+    const float2 f2 = half2_bits_to_float2(b2), f3 = half2_bits_to_float2(b3);
+    lo = 0.f;
+    lo += f0.x;
+    lo += f1.x;
+    lo += f0.y;
+    lo += f1.y;
+    hi = 0.f;
+    hi += f2.x;
+    hi += f3.x;
+    hi += f2.y;
+    hi += f3.y;
+    return make_uint4(b0, b1, b2, b3);
+  }
+}
+
+// The two loads of one entry (see q_entry) from query row qr (fp32, kD values).
+template <int KT>
+__device__ __forceinline__ void q_entry_load(const float* qr, int kp, int t, float4& v0, float4& v1) {
+  if constexpr (KT == PA_F16) {
+    const float* r = qr + 32 * kp + 2 * t;
+    const float2 a = __ldg(reinterpret_cast<const float2*>(r)), b = __ldg(reinterpret_cast<const float2*>(r + 8));
+    const float2 c = __ldg(reinterpret_cast<const float2*>(r + 16)), d = __ldg(reinterpret_cast<const float2*>(r + 24));
+    v0 = make_float4(a.x, a.y, b.x, b.y);
+    v1 = make_float4(c.x, c.y, d.x, d.y);
+  } else {
+    const float* r = qr + 32 * kp + 4 * t;
+    v0 = __ldg(reinterpret_cast<const float4*>(r));
+    v1 = __ldg(reinterpret_cast<const float4*>(r + 16));
+  }
+}
+
+// Block bias of a quantised K format from the quad-reduced halves: the magic
+// bias the raw K halves carry, times Q.
+template <int KT>
+__device__ __forceinline__ float q_block_bias(float lo, float hi) {
+  return (KT == PA_Q4_0) ? 1032.f * lo + 1152.f * hi : 1152.f * (lo + hi);
+}
+
 // Head-group path: warp w stages its own KV head's six query rows (one query
 // token) as S-MMA B fragments and the block biases ([block][t] float4), from
 // coalesced float4 loads.  Rows 6 and 7 of the fragment (padding) are zero.
@@ -609,68 +666,41 @@ __device__ __forceinline__ const float* q_row(const DecodeParams& p, int s, int 
 // Per-head path: stage Q of (sequence s, KV head g) as S-MMA B fragments in
 // the K format's dim order (high-nibble Q4_0 k-steps hold Q/16) and, for
 // quantised K, the block biases ([block][nt][t] float4).  The 128 threads of
-// one consumer group (tid 0..127) take part: the R query rows from segment row
-// row0 on (1 KB each) are read as float4, all of a thread's loads in flight at
-// once; rows R .. 8*NT-1 of the fragments and biases are zero.
+// one consumer group (tid 0..127) take part: thread tid builds fragment
+// entries tid + 128 i, i.e. (k-step pair, n-tile) warp + 4 i, lane (g, t):
+// query row nt * 8 + g of the R rows from segment row row0 on (rows R ..
+// 8*NT-1 are zero), all of its loads in flight at once.
 template <int KT, int NT>
 __device__ __noinline__ void stage_q(const DecodeParams& p, int s, int g, uint32_t qf, float* cb4, int tid, int row0,
                                      int R) {
-  constexpr int kN = kCWarps * 32;
-  constexpr int kLoads = (NT * 8 * kD / 4 + kN - 1) / kN;  // float4 per thread covering 8*NT rows
-  const int lane = tid & 31;
-  // zero the padding rows: fragment lanes (row % 8) * 4 + t of n-tile row / 8
-  for (int e = tid; e < 8 * NT * 32; e += kN) {  // (k-step pair, nt, lane)
-    const int ln = e & 31, nt = (e >> 5) % NT, kp = e / (32 * NT);
-    if (nt * 8 + (ln >> 2) >= R) sts128_zero(qf + ((kp * NT + nt) * 32 + ln) * 16);
-  }
-  if (KT != PA_F16) {
-    for (int e = tid; e < 8 * NT * 8; e += kN) {  // (block, row) pairs of padding rows
-      const int blk = e / (NT * 8), row = e % (NT * 8);
-      if (row >= R) {
-        float* c = cb4 + ((blk * NT + (row >> 3)) * 4 + ((row & 7) >> 1)) * 4 + (row & 1);
-        c[0] = 0.f;
-        c[2] = 0.f;
-      }
+  constexpr int kE = 8 * NT * 32 / (kCWarps * 32);  // entries per thread
+  const int lane = tid & 31, t = lane & 3, gq = lane >> 2, warp = tid >> 5;
+  float4 v0[kE], v1[kE];
+#pragma unroll
+  for (int i = 0; i < kE; ++i) {
+    const int q = warp + kCWarps * i, kp = q / NT, row = (q % NT) * 8 + gq;
+    if (row < R) {
+      q_entry_load<KT>(q_row(p, s, g, row0 + row), kp, t, v0[i], v1[i]);
+    } else {
+      v0[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      v1[i] = v0[i];
     }
   }
-  float4 qv[kLoads];
 #pragma unroll
-  for (int i = 0; i < kLoads; ++i) {
-    const int f = tid + kN * i, row = f >> 6;
-    qv[i] = row < R ? __ldg(reinterpret_cast<const float4*>(q_row(p, s, g, row0 + row)) + (f & 63))
-                    : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-#pragma unroll
-  for (int i = 0; i < kLoads; ++i) {
-    const int f = tid + kN * i, row = f >> 6, d0 = 4 * (f & 63);
-    const float vals[4] = {qv[i].x, qv[i].y, qv[i].z, qv[i].w};
-    float lo = 0.f;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      int ks, jj;
-      const int t = kdim_inverse<KT>(d0 + k, ks, jj);
-      const float sc = (KT == PA_Q4_0 && (ks & 1)) ? 0.0625f : 1.f;
-      const __half hv = __float2half_rn(sc * vals[k]);
-      lo += __half2float(hv);
-      if (row < R) {
-        const int ln = 4 * (row & 7) + t;
-        const uint32_t addr =
-            qf + (((ks >> 1) * NT + (row >> 3)) * 32 + ln) * 16 + (ks & 1) * 8 + ((jj >> 3) << 2) + ((jj & 1) << 1);
-        asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(__half_as_ushort(hv)) : "memory");
-      }
-    }
-    if (KT != PA_F16) {
-      // Lanes 8m .. 8m+7 hold the eight float4 of one 32-dim block of one row
-      // (k < 4: its low 16 dims, k >= 4: its high 16 dims).
+  for (int i = 0; i < kE; ++i) {
+    const int q = warp + kCWarps * i, kp = q / NT, nt = q % NT, row = nt * 8 + gq;
+    float lo, hi;
+    sts128(qf + (q * 32 + lane) * 16, q_entry<KT>(v0[i], v1[i], lo, hi));
+    if constexpr (KT != PA_F16) {
       lo += __shfl_xor_sync(0xffffffffu, lo, 1);
       lo += __shfl_xor_sync(0xffffffffu, lo, 2);
-      const float hi = __shfl_down_sync(0xffffffffu, lo, 4);
-      if ((lane & 7) == 0 && row < R) {
-        const int blk = (f & 63) >> 3;
-        const float c = (KT == PA_Q4_0) ? 1032.f * lo + 1152.f * hi : 1152.f * (lo + hi);
-        float* e = cb4 + ((blk * NT + (row >> 3)) * 4 + ((row & 7) >> 1)) * 4 + (row & 1);
-        e[0] = -c;
-        e[2] = -c;
+      hi += __shfl_xor_sync(0xffffffffu, hi, 1);
+      hi += __shfl_xor_sync(0xffffffffu, hi, 2);
+      if (t == 0) {
+        const float c = row < R ? -q_block_bias<KT>(lo, hi) : 0.f;
+        float* e = cb4 + ((kp * NT + nt) * 4 + (gq >> 1)) * 4 + (gq & 1);
+        e[0] = c;
+        e[2] = c;
       }
     }
   }
