@@ -17,6 +17,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "pa.h"
 #include "pa_rows_tc.cuh"
@@ -224,6 +225,10 @@ bool lookup_rows_tc_kernel(int kt, int vt, KernelInfo* out) {
 // kernels (measured: the decode kernels are faster up to eight tokens).
 constexpr uint32_t kRowsFromQTok = 9;
 
+// Extra cost, in tiles, of a piece's first tile in the 2-8-token CTA split
+// (cta_first_tile).
+constexpr int kPieceCost = 2;
+
 // The split kernel for n_qtok query tokens: the decode kernels below
 // kRowsFromQTok tokens (by n-tiles of 8 query rows), the row-tile kernel from
 // there to 96.  *slot: its index in the occupancy cache.
@@ -333,6 +338,7 @@ struct Plan {
   Geometry geo;
   long long tiles;
   int ctas;
+  int piece_cost;  // w of cta_first_tile
   long long n_seg;
   long long slots;
   int merge_tasks;
@@ -342,8 +348,23 @@ struct Plan {
 // List the merge tasks (every segment with more than one piece) into task[];
 // returns their number, or -1 past kMaxTasks.  *n_items gets the number of
 // work items (CTAs of the merge grid).
+// The CTAs' first tiles (the split kernel's own cuts), ctas + 1 entries.
+std::vector<long long> cta_cuts(const int32_t* seq_lens_host, uint32_t n_seq, const Geometry& geo, long long tiles,
+                                int ctas, int piece_cost) {
+  std::vector<long long> cut(ctas + 1);
+  for (int i = 0; i <= ctas; ++i)
+    cut[i] = cta_first_tile(seq_lens_host, (int)n_seq, geo.segs_per_seq, geo.tile_keys, tiles, ctas, piece_cost, i);
+  return cut;
+}
+
+// The CTA whose range holds tile x.
+int cta_of(const std::vector<long long>& cut, long long x) {
+  return (int)(std::upper_bound(cut.begin(), cut.end(), x) - cut.begin()) - 1;
+}
+
 int list_merge_tasks(const int32_t* seq_lens_host, uint32_t n_seq, uint32_t n_qtok, const Geometry& geo,
-                     long long tiles, int ctas, MergeTask* task, long long* n_items) {
+                     long long tiles, int ctas, int piece_cost, MergeTask* task, long long* n_items) {
+  const std::vector<long long> cut = cta_cuts(seq_lens_host, n_seq, geo, tiles, ctas, piece_cost);
   int n = 0;
   long long items = 0;
   long long base = 0;
@@ -352,7 +373,7 @@ int list_merge_tasks(const int32_t* seq_lens_host, uint32_t n_seq, uint32_t n_qt
       const long long ntl = seg_tiles(geo, seq_lens_host[s], n_qtok, g);
       const long long a = base, e = a + ntl - 1;
       base += ntl;
-      const int c0 = (int)(((a + 1) * ctas - 1) / tiles), c1 = (int)(((e + 1) * ctas - 1) / tiles);
+      const int c0 = cta_of(cut, a), c1 = cta_of(cut, e);
       const int np = c1 - c0 + 1;
       if (np < 2) continue;
       if (n == kMaxTasks) return -1;
@@ -419,12 +440,18 @@ static pa_status make_plan(const pa_pool_desc& d, const int32_t* seq_lens_host, 
   plan->geo = geo;
   plan->tiles = tiles;
   plan->ctas = (int)std::min<long long>(tiles, (long long)sms * occ);
+  // Two to eight query tokens: a new piece costs about two tiles of work
+  // (staging its query rows, writing its partial), so ranges that hold
+  // segment starts get fewer tiles -- when every range keeps at least one.
+  plan->piece_cost =
+      (geo.n_row_tiles == 0 && n_qtok >= 2 && tiles >= (long long)plan->ctas * (1 + kPieceCost)) ? kPieceCost : 0;
   plan->n_seg = (long long)n_seq * geo.segs_per_seq;
   plan->slots = (long long)plan->ctas + plan->n_seg;
   // Each multi-piece segment holds a CTA boundary, so there are fewer merge
   // tasks than CTAs: kMaxTasks covers any grid of up to 1024 CTAs.
   plan->merge_tasks =
-      list_merge_tasks(seq_lens_host, n_seq, n_qtok, geo, tiles, plan->ctas, nullptr, &plan->merge_items);
+      list_merge_tasks(seq_lens_host, n_seq, n_qtok, geo, tiles, plan->ctas, plan->piece_cost, nullptr,
+                       &plan->merge_items);
   if (plan->merge_tasks < 0 || plan->merge_items >= (1ll << 31)) return PA_ERR_UNSUPPORTED;
   return PA_OK;
 }
@@ -452,15 +479,14 @@ extern "C" pa_status pa_decode_plan(const pa_pool* pool, const int32_t* seq_lens
     tiles += (uint32_t)plan.tiles;
     keys = (uint32_t)geo.tile_keys;
     // Pieces = CTA-range cuts plus segment cuts.
+    const std::vector<long long> cut = cta_cuts(lens, cn, geo, plan.tiles, plan.ctas, plan.piece_cost);
     long long base = 0;
     for (uint32_t s = 0; s < cn; ++s) {
       for (int g = 0; g < geo.segs_per_seq; ++g) {
         const long long ntl = seg_tiles(geo, lens[s], n_qtok, g);
         const long long a = base, e = a + ntl - 1;
         base += ntl;
-        const int c0p = (int)(((a + 1) * plan.ctas - 1) / plan.tiles);
-        const int c1p = (int)(((e + 1) * plan.ctas - 1) / plan.tiles);
-        pieces += (uint32_t)(c1p - c0p + 1);
+        pieces += (uint32_t)(cta_of(cut, e) - cta_of(cut, a) + 1);
       }
     }
   }
@@ -518,6 +544,7 @@ static pa_status prepare_decode(const pa_pool* pool, const float* q, const void*
   p.part_o = reinterpret_cast<float*>(ws + lay.o);
   p.total_tiles = plan->tiles;
   p.n_ctas = plan->ctas;
+  p.piece_cost = plan->piece_cost;
   p.n_seq = (int)n_seq;
   p.n_qtok = (int)n_qtok;
   p.n_kv_heads = (int)d.n_kv_heads;
@@ -552,7 +579,8 @@ static pa_status launch_merge(const DecodeParams& p, const Plan& plan, const int
   static thread_local MergeParams<kCap> mp;  // up to 20 KB: kept off the stack
   mp.p = MergeCore{p.part_ml, p.part_o, p.out, p.lse, p.n_qtok, p.n_q_heads, p.seg_heads, p.segs_per_seq,
                    p.rows_per_seg, p.n_row_tiles};
-  mp.n_tasks = list_merge_tasks(seq_lens_host, n_seq, (uint32_t)p.n_qtok, plan.geo, plan.tiles, plan.ctas, mp.task,
+  mp.n_tasks = list_merge_tasks(seq_lens_host, n_seq, (uint32_t)p.n_qtok, plan.geo, plan.tiles, plan.ctas,
+                                plan.piece_cost, mp.task,
                                 nullptr);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)plan.merge_items);

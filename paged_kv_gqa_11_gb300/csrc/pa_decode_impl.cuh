@@ -96,6 +96,37 @@ constexpr int kAlign = 512;    // stage-ring alignment the chunk addressing reli
 // parameters, and larger batches run as consecutive sub-batches.
 constexpr int kInlineSeqs = 128;
 
+// First tile of CTA i when the launch's T tiles are cut into G contiguous
+// ranges of equal cost: a tile costs 1, and the first tile of each segment
+// costs w more (the work of a new piece: staging its query rows, writing its
+// partial).  Segment order is (sequence, segment-in-sequence); every segment
+// of sequence s holds ceil(lens[s] / tile_keys) tiles.  w = 0 gives the equal
+// cut i * T / G.  With w > 0 the caller ensures T >= G (1 + w), so that
+// consecutive cuts differ by at least one tile.  The cut depends only on the
+// lengths, never on page size or placement.
+__host__ __device__ inline long long cta_first_tile(const int32_t* lens, int n_seq, int segs, int tile_keys,
+                                                    long long T, int G, int w, int i) {
+  if (w == 0) return (long long)i * T / G;
+  const long long C = T + (long long)w * n_seq * segs;  // total cost
+  const long long c = (long long)i * C / G;             // the cost before CTA i's first tile
+  if (c <= 0) return 0;
+  // Cost of tiles [0, x): C(x) = x + w * (segments starting below x).  The
+  // smallest x with C(x) >= c lies in the segment k whose tiles (st_k, st_k +
+  // n] (as cut positions) reach c: there C(x) = x + w (k + 1).
+  long long st = 0, k0 = 0;  // first tile and first segment of sequence s
+  for (int s = 0; s < n_seq; ++s) {
+    const long long n = (lens[s] + tile_keys - 1) / tile_keys;
+    if (c <= st + segs * n + w * (k0 + segs)) {
+      const long long j = (c - st - w * k0 + n + w - 1) / (n + w) - 1;  // segment of this sequence
+      const long long x = c - w * (k0 + j + 1), lo = st + j * n + 1;
+      return x > lo ? x : lo;
+    }
+    st += segs * n;
+    k0 += segs;
+  }
+  return T;
+}
+
 // ------------------------------------------------------------------ stage geometry
 
 // A stage holds four row groups of K then four of V: 16 keys x 4 heads (one
@@ -245,6 +276,7 @@ struct DecodeParams {
   int rows_per_seg;  // query rows per segment: 6 * seg_heads * n_qtok, or a row tile
   int n_row_tiles;   // row tiles per KV head (9 to 96 query tokens), else 0
   float scale_log2;  // scale * log2(e)
+  int piece_cost;    // w of cta_first_tile (0: equal tile ranges)
   // The host copy of the lengths (n_seq <= kInlineSeqs).  The tile walk, the
   // table reads and the masks use only these, so nothing the device copy
   // holds can move a read out of a sequence's table row; seq_lens (device) is
@@ -277,7 +309,7 @@ struct Smem {
   static constexpr int kGrpBytes = kStat + 2 * kCWarps * NT * 8 * 8 - kQ;
   static constexpr int kWorkEnd = NT == 1 ? kWCb + kCWarps * kWCbBytes : kQ + kG * kGrpBytes;
   static constexpr int kBar = kWorkEnd;                 // full[kStages], empty[kStages]
-  static constexpr int kMisc = kBar + 2 * kStages * 8;  // abort flag, start position
+  static constexpr int kMisc = kBar + 2 * kStages * 8;  // abort flag, start position, tile range
   static constexpr int kTotal = kMisc + 32;
   static constexpr int kLaunch = kTotal + kAlign;  // dynamic bytes requested (base aligned inside)
 };
@@ -1395,10 +1427,8 @@ __global__ void __launch_bounds__(threads_of(kG), CtaTarget<KT, VT, NT, kG>::kN)
   const uint32_t bar_full = ring + SM::kBar, bar_empty = bar_full + 8 * kStages;
   volatile int* abort = reinterpret_cast<volatile int*>(smem + SM::kMisc);
   int* start = reinterpret_cast<int*>(smem + SM::kMisc + 4);
+  long long* range = reinterpret_cast<long long*>(smem + SM::kMisc + 16);
 
-  const long long T = p.total_tiles;
-  const int Gn = p.n_ctas;
-  const long long a = (long long)blockIdx.x * T / Gn, b = (long long)(blockIdx.x + 1) * T / Gn;
   // Launched as a programmatic dependent of the previous kernel on the stream
   // (for example the append of this step's rows): every thread waits for it
   // to complete before it reads any input.
@@ -1414,15 +1444,23 @@ __global__ void __launch_bounds__(threads_of(kG), CtaTarget<KT, VT, NT, kG>::kN)
       mbar_init(bar_empty + 8 * i, NT == 1 ? p.seg_heads : kCWarps * kG);  // one arrival per consuming warp
     }
     fence_mbar_init();
+    // This CTA's tile range [a, b) (the host plan lists the same cuts).
+    const int i = (int)blockIdx.x;
+    const long long a0 =
+        cta_first_tile(p.lens, p.n_seq, p.segs_per_seq, p.tile_keys, p.total_tiles, p.n_ctas, p.piece_cost, i);
+    range[0] = a0;
+    range[1] =
+        cta_first_tile(p.lens, p.n_seq, p.segs_per_seq, p.tile_keys, p.total_tiles, p.n_ctas, p.piece_cost, i + 1);
     int s0, g0, j0;
-    locate_tile(p, a, s0, g0, j0);
+    locate_tile(p, a0, s0, g0, j0);
     start[0] = s0;
     start[1] = g0;
     start[2] = j0;
   }
   __syncthreads();
+  const long long a = range[0], b = range[1];
   const int s = start[0], g = start[1], j = start[2];
-  if (s >= p.n_seq) return;  // an empty range (the planner gives every CTA a tile)
+  if (s >= p.n_seq || a >= b) return;  // an empty range (the planner gives every CTA a tile)
 
   if (warp == kCWarps * kG) {
     TilePos pos;
