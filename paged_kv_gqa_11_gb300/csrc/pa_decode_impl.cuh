@@ -803,10 +803,20 @@ __device__ __forceinline__ void s_phase(float (&acc)[NT][4], uint32_t kq, uint32
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           const float4 c = lds128f(cbl + (b * NT + nt) * 64);
-          float tmp[4] = {c.x, c.y, c.z, c.w};
           const uint4 q = lds128(qf + (b * NT + nt) * 512);
-          mma_16816(tmp, a0, q.x, q.y);
-          mma_16816(tmp, a1, q.z, q.w);
+          float tmp[4] = {c.x, c.y, c.z, c.w};
+          if constexpr (NT >= 4) {
+            // One CTA per SM has the registers for two independent MMA
+            // chains per block (measured faster there, neutral below).
+            float tm2[4] = {0.f, 0.f, 0.f, 0.f};
+            mma_16816(tmp, a0, q.x, q.y);
+            mma_16816(tm2, a1, q.z, q.w);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) tmp[e] += tm2[e];
+          } else {
+            mma_16816(tmp, a0, q.x, q.y);
+            mma_16816(tmp, a1, q.z, q.w);
+          }
           acc[nt][0] = fmaf(d0, tmp[0], acc[nt][0]);
           acc[nt][1] = fmaf(d0, tmp[1], acc[nt][1]);
           acc[nt][2] = fmaf(d1, tmp[2], acc[nt][2]);
@@ -1428,6 +1438,10 @@ __global__ void __launch_bounds__(threads_of(kG), CtaTarget<KT, VT, NT, kG>::kN)
   volatile int* abort = reinterpret_cast<volatile int*>(smem + SM::kMisc);
   int* start = reinterpret_cast<int*>(smem + SM::kMisc + 4);
   long long* range = reinterpret_cast<long long*>(smem + SM::kMisc + 16);
+  // This CTA's tile range [a, b), the host plan's cuts: equal tile counts in
+  // closed form, or (piece_cost > 0) the weighted cut, walked by thread 0.
+  const int cta = (int)blockIdx.x;
+  long long a = (long long)cta * p.total_tiles / p.n_ctas, b = (long long)(cta + 1) * p.total_tiles / p.n_ctas;
 
   // Launched as a programmatic dependent of the previous kernel on the stream
   // (for example the append of this step's rows): every thread waits for it
@@ -1444,21 +1458,24 @@ __global__ void __launch_bounds__(threads_of(kG), CtaTarget<KT, VT, NT, kG>::kN)
       mbar_init(bar_empty + 8 * i, NT == 1 ? p.seg_heads : kCWarps * kG);  // one arrival per consuming warp
     }
     fence_mbar_init();
-    // This CTA's tile range [a, b) (the host plan lists the same cuts).
-    const int i = (int)blockIdx.x;
-    const long long a0 =
-        cta_first_tile(p.lens, p.n_seq, p.segs_per_seq, p.tile_keys, p.total_tiles, p.n_ctas, p.piece_cost, i);
-    range[0] = a0;
-    range[1] =
-        cta_first_tile(p.lens, p.n_seq, p.segs_per_seq, p.tile_keys, p.total_tiles, p.n_ctas, p.piece_cost, i + 1);
+    if (p.piece_cost) {
+      a = cta_first_tile(p.lens, p.n_seq, p.segs_per_seq, p.tile_keys, p.total_tiles, p.n_ctas, p.piece_cost, cta);
+      b = cta_first_tile(p.lens, p.n_seq, p.segs_per_seq, p.tile_keys, p.total_tiles, p.n_ctas, p.piece_cost,
+                         cta + 1);
+      range[0] = a;
+      range[1] = b;
+    }
     int s0, g0, j0;
-    locate_tile(p, a0, s0, g0, j0);
+    locate_tile(p, a, s0, g0, j0);
     start[0] = s0;
     start[1] = g0;
     start[2] = j0;
   }
   __syncthreads();
-  const long long a = range[0], b = range[1];
+  if (p.piece_cost) {
+    a = range[0];
+    b = range[1];
+  }
   const int s = start[0], g = start[1], j = start[2];
   if (s >= p.n_seq || a >= b) return;  // an empty range (the planner gives every CTA a tile)
 

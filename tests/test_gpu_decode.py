@@ -298,6 +298,34 @@ def test_plan_covers_every_tile():
         assert plan["partials"] >= w.n_seq * segs
 
 
+def _weighted_pieces(lens, keys, segs, ctas, w):
+    """Pieces of the CTA cut over a cost where a tile costs 1 and a segment's
+    first tile w more, by brute force: CTA i starts at the smallest x whose
+    cost of tiles [0, x) reaches floor(i * total / ctas)."""
+    n = [(L + keys - 1) // keys for L in lens for _ in range(segs)]
+    starts = np.cumsum([0] + n[:-1])
+    T = int(sum(n))
+    cost = np.arange(T + 1) + w * np.searchsorted(starts, np.arange(T + 1), side="left")
+    total = T + w * len(n)
+    cut = [int(np.argmax(cost >= (i * total) // ctas)) for i in range(ctas)] + [T]
+    assert all(b > a for a, b in zip(cut, cut[1:]))
+    owner = np.searchsorted(cut, np.arange(T), side="right") - 1
+    return sum(int(owner[s + k - 1]) - int(owner[s]) + 1 for s, k in zip(starts, n))
+
+
+def test_plan_weights_segment_starts():
+    """Two to eight query tokens: the CTA ranges are cut at equal cost with a
+    segment's first tile weighing two tiles more, so ranges that hold segment
+    starts get fewer tiles; one token keeps equal tile counts."""
+    c = PagedKVCache(8, 256, W.TYPE_Q8_0, W.TYPE_Q8_0)
+    mixed = [9000] * 3 + [130] * 100  # many segment starts
+    for lens, nq, keys, segs, w in ((W.VERIFY_LENGTHS, 1, 16, 1, 0), (W.VERIFY_LENGTHS, 3, 64, W.HKV, 2),
+                                    (W.VERIFY_LENGTHS, 8, 64, W.HKV, 2), (mixed, 3, 64, W.HKV, 2)):
+        plan = pa_decode_plan(c.pool, lens, nq)
+        assert plan["partials"] == _weighted_pieces(lens, keys, segs, plan["ctas"], w), (nq, plan)
+    assert plan["partials"] != _weighted_pieces(mixed, 64, W.HKV, plan["ctas"], 0)
+
+
 def test_prefix_fork_with_copy_on_write():
     """Sequence A (100 rows) is forked into B by sharing its blocks.  B's
     partly filled last page is copied on write before B appends 20 rows; A
