@@ -803,8 +803,8 @@ __device__ __forceinline__ void s_phase(float (&acc)[NT][4], uint32_t kq, uint32
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           const float4 c = lds128f(cbl + (b * NT + nt) * 64);
-          const uint4 q = lds128(qf + (b * NT + nt) * 512);
           float tmp[4] = {c.x, c.y, c.z, c.w};
+          const uint4 q = lds128(qf + (b * NT + nt) * 512);
           if constexpr (NT >= 4) {
             // One CTA per SM has the registers for two independent MMA
             // chains per block (measured faster there, neutral below).
@@ -1439,7 +1439,8 @@ __global__ void __launch_bounds__(threads_of(kG), CtaTarget<KT, VT, NT, kG>::kN)
   int* start = reinterpret_cast<int*>(smem + SM::kMisc + 4);
   long long* range = reinterpret_cast<long long*>(smem + SM::kMisc + 16);
   // This CTA's tile range [a, b), the host plan's cuts: equal tile counts in
-  // closed form, or (piece_cost > 0) the weighted cut, walked by thread 0.
+  // closed form, or (2-8 tokens, piece_cost > 0) the weighted cut, walked by
+  // thread 0.
   const int cta = (int)blockIdx.x;
   long long a = (long long)cta * p.total_tiles / p.n_ctas, b = (long long)(cta + 1) * p.total_tiles / p.n_ctas;
 
@@ -1458,7 +1459,7 @@ __global__ void __launch_bounds__(threads_of(kG), CtaTarget<KT, VT, NT, kG>::kN)
       mbar_init(bar_empty + 8 * i, NT == 1 ? p.seg_heads : kCWarps * kG);  // one arrival per consuming warp
     }
     fence_mbar_init();
-    if (p.piece_cost) {
+    if (NT > 1 && p.piece_cost) {
       a = cta_first_tile(p.lens, p.n_seq, p.segs_per_seq, p.tile_keys, p.total_tiles, p.n_ctas, p.piece_cost, cta);
       b = cta_first_tile(p.lens, p.n_seq, p.segs_per_seq, p.tile_keys, p.total_tiles, p.n_ctas, p.piece_cost,
                          cta + 1);
@@ -1472,12 +1473,12 @@ __global__ void __launch_bounds__(threads_of(kG), CtaTarget<KT, VT, NT, kG>::kN)
     start[2] = j0;
   }
   __syncthreads();
-  if (p.piece_cost) {
+  if (NT > 1 && p.piece_cost) {
     a = range[0];
     b = range[1];
   }
   const int s = start[0], g = start[1], j = start[2];
-  if (s >= p.n_seq || a >= b) return;  // an empty range (the planner gives every CTA a tile)
+  if (s >= p.n_seq) return;  // an empty range (the planner gives every CTA a tile)
 
   if (warp == kCWarps * kG) {
     TilePos pos;
