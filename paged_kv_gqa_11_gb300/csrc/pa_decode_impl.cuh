@@ -802,9 +802,19 @@ __device__ __forceinline__ void s_phase(float (&acc)[NT][4], uint32_t kq, uint32
         const float d0 = hb ? dA.y : dA.x, d1 = hb ? dB.y : dB.x;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
+          // (The statement order here steers the compiler's schedule: both
+          // loads before the accumulator is seeded measured 4 % faster from
+          // two n-tiles on, the seed between them faster for one.)
           const float4 c = lds128f(cbl + (b * NT + nt) * 64);
-          float tmp[4] = {c.x, c.y, c.z, c.w};
-          const uint4 q = lds128(qf + (b * NT + nt) * 512);
+          uint4 q;
+          float tmp[4];
+          if constexpr (NT == 1) {
+            tmp[0] = c.x, tmp[1] = c.y, tmp[2] = c.z, tmp[3] = c.w;
+            q = lds128(qf + (b * NT + nt) * 512);
+          } else {
+            q = lds128(qf + (b * NT + nt) * 512);
+            tmp[0] = c.x, tmp[1] = c.y, tmp[2] = c.z, tmp[3] = c.w;
+          }
           if constexpr (NT >= 4) {
             // One CTA per SM has the registers for two independent MMA
             // chains per block (measured faster there, neutral below).
