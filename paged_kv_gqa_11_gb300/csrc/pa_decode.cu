@@ -345,15 +345,34 @@ struct Plan {
   long long merge_items;  // CTAs of the merge grid
 };
 
-// List the merge tasks (every segment with more than one piece) into task[];
-// returns their number, or -1 past kMaxTasks.  *n_items gets the number of
-// work items (CTAs of the merge grid).
-// The CTAs' first tiles (the split kernel's own cuts), ctas + 1 entries.
+// The CTAs' first tiles (the split kernel's own cuts, cta_first_tile), ctas + 1
+// entries, in one walk over the sequences: the targets only grow.
 std::vector<long long> cta_cuts(const int32_t* seq_lens_host, uint32_t n_seq, const Geometry& geo, long long tiles,
                                 int ctas, int piece_cost) {
   std::vector<long long> cut(ctas + 1);
-  for (int i = 0; i <= ctas; ++i)
-    cut[i] = cta_first_tile(seq_lens_host, (int)n_seq, geo.segs_per_seq, geo.tile_keys, tiles, ctas, piece_cost, i);
+  const int w = piece_cost, segs = geo.segs_per_seq;
+  if (w == 0) {
+    for (int i = 0; i <= ctas; ++i) cut[i] = (long long)i * tiles / ctas;
+    return cut;
+  }
+  const long long total = tiles + (long long)w * n_seq * segs;
+  uint32_t s = 0;
+  long long st = 0, k0 = 0;
+  for (int i = 0; i <= ctas; ++i) {
+    const long long c = (long long)i * total / ctas;
+    if (c <= 0) {
+      cut[i] = 0;
+      continue;
+    }
+    long long n = 0;
+    for (; s < n_seq; ++s) {
+      n = (seq_lens_host[s] + geo.tile_keys - 1) / geo.tile_keys;
+      if (cut_falls_in(c, st, k0, n, segs, w)) break;
+      st += segs * n;
+      k0 += segs;
+    }
+    cut[i] = s < n_seq ? cut_in_sequence(c, st, k0, n, w) : tiles;
+  }
   return cut;
 }
 
@@ -362,6 +381,9 @@ int cta_of(const std::vector<long long>& cut, long long x) {
   return (int)(std::upper_bound(cut.begin(), cut.end(), x) - cut.begin()) - 1;
 }
 
+// List the merge tasks (every segment with more than one piece) into task[];
+// returns their number, or -1 past kMaxTasks.  *n_items gets the number of
+// work items (CTAs of the merge grid).
 int list_merge_tasks(const int32_t* seq_lens_host, uint32_t n_seq, uint32_t n_qtok, const Geometry& geo,
                      long long tiles, int ctas, int piece_cost, MergeTask* task, long long* n_items) {
   const std::vector<long long> cut = cta_cuts(seq_lens_host, n_seq, geo, tiles, ctas, piece_cost);

@@ -96,31 +96,41 @@ constexpr int kAlign = 512;    // stage-ring alignment the chunk addressing reli
 // parameters, and larger batches run as consecutive sub-batches.
 constexpr int kInlineSeqs = 128;
 
-// First tile of CTA i when the launch's T tiles are cut into G contiguous
-// ranges of equal cost: a tile costs 1, and the first tile of each segment
-// costs w more (the work of a new piece: staging its query rows, writing its
-// partial).  Segment order is (sequence, segment-in-sequence); every segment
-// of sequence s holds ceil(lens[s] / tile_keys) tiles.  w = 0 gives the equal
-// cut i * T / G.  With w > 0 the caller ensures T >= G (1 + w), so that
+// The CTA split.  A launch's T tiles, laid end to end in segment order
+// (sequence, segment-in-sequence), are cut into G contiguous ranges of equal
+// cost: a tile costs 1, and the first tile of each segment costs w more (the
+// work of a new piece: staging its query rows, writing its partial).  Every
+// segment of sequence s holds ceil(lens[s] / tile_keys) tiles.  The cost of
+// tiles [0, x) is C(x) = x + w * (segments starting below x); CTA i starts at
+// the smallest x with C(x) >= floor(i * C(T) / G).  w = 0 gives the equal cut
+// i * T / G.  With w > 0 the caller ensures T >= G (1 + w), so that
 // consecutive cuts differ by at least one tile.  The cut depends only on the
 // lengths, never on page size or placement.
+
+// Target cost c falls in sequence s (first tile st, first segment k0, segs
+// segments of n tiles) when c <= C(end of s).
+__host__ __device__ inline bool cut_falls_in(long long c, long long st, long long k0, long long n, int segs, int w) {
+  return c <= st + segs * n + (long long)w * (k0 + segs);
+}
+
+// The cut for target c > C(st) inside sequence s: segment j of the sequence
+// spans cuts (st + j n, st + (j + 1) n], where C(x) = x + w (k0 + j + 1).
+__host__ __device__ inline long long cut_in_sequence(long long c, long long st, long long k0, long long n, int w) {
+  const long long j = (c - st - w * k0 + n + w - 1) / (n + w) - 1;
+  const long long x = c - w * (k0 + j + 1), lo = st + j * n + 1;
+  return x > lo ? x : lo;
+}
+
+// First tile of CTA i (walked from the first sequence).
 __host__ __device__ inline long long cta_first_tile(const int32_t* lens, int n_seq, int segs, int tile_keys,
                                                     long long T, int G, int w, int i) {
   if (w == 0) return (long long)i * T / G;
-  const long long C = T + (long long)w * n_seq * segs;  // total cost
-  const long long c = (long long)i * C / G;             // the cost before CTA i's first tile
+  const long long c = (long long)i * (T + (long long)w * n_seq * segs) / G;
   if (c <= 0) return 0;
-  // Cost of tiles [0, x): C(x) = x + w * (segments starting below x).  The
-  // smallest x with C(x) >= c lies in the segment k whose tiles (st_k, st_k +
-  // n] (as cut positions) reach c: there C(x) = x + w (k + 1).
   long long st = 0, k0 = 0;  // first tile and first segment of sequence s
   for (int s = 0; s < n_seq; ++s) {
     const long long n = (lens[s] + tile_keys - 1) / tile_keys;
-    if (c <= st + segs * n + w * (k0 + segs)) {
-      const long long j = (c - st - w * k0 + n + w - 1) / (n + w) - 1;  // segment of this sequence
-      const long long x = c - w * (k0 + j + 1), lo = st + j * n + 1;
-      return x > lo ? x : lo;
-    }
+    if (cut_falls_in(c, st, k0, n, segs, w)) return cut_in_sequence(c, st, k0, n, w);
     st += segs * n;
     k0 += segs;
   }
@@ -802,19 +812,9 @@ __device__ __forceinline__ void s_phase(float (&acc)[NT][4], uint32_t kq, uint32
         const float d0 = hb ? dA.y : dA.x, d1 = hb ? dB.y : dB.x;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          // (The statement order here steers the compiler's schedule: both
-          // loads before the accumulator is seeded measured 4 % faster from
-          // two n-tiles on, the seed between them faster for one.)
           const float4 c = lds128f(cbl + (b * NT + nt) * 64);
-          uint4 q;
-          float tmp[4];
-          if constexpr (NT == 1) {
-            tmp[0] = c.x, tmp[1] = c.y, tmp[2] = c.z, tmp[3] = c.w;
-            q = lds128(qf + (b * NT + nt) * 512);
-          } else {
-            q = lds128(qf + (b * NT + nt) * 512);
-            tmp[0] = c.x, tmp[1] = c.y, tmp[2] = c.z, tmp[3] = c.w;
-          }
+          float tmp[4] = {c.x, c.y, c.z, c.w};
+          const uint4 q = lds128(qf + (b * NT + nt) * 512);
           if constexpr (NT >= 4) {
             // One CTA per SM has the registers for two independent MMA
             // chains per block (measured faster there, neutral below).
