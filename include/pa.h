@@ -301,7 +301,11 @@ size_t pa_decode_workspace_size(const pa_pool* pool, uint32_t n_seq, uint32_t n_
  * context is split across the GPU by occupancy, adaptively for long
  * contexts): *n_ctas decode CTAs (the largest grid over the sub-batches),
  * *n_tiles key tiles of `*tile_keys` keys each in total, and *n_partials
- * split partials (pieces).  Host only, nothing launched; for tests and tools.
+ * split partials (pieces).  The tiles, laid end to end by (sequence, KV
+ * head), are cut into contiguous per-CTA ranges: of equal tile counts for one
+ * query token and for row tiles; for 2-8 tokens of equal cost, where the first
+ * tile of each (sequence, KV head) counts two tiles more, whenever every range
+ * still gets a tile.  Host only, nothing launched; for tests and tools.
  * PA_ERR_INVALID for a null pool or lengths, n_seq = 0 or a length below
  * n_qtok; PA_ERR_UNSUPPORTED for a shape pa_decode does not take. */
 pa_status pa_decode_plan(const pa_pool* pool, const int32_t* seq_lens_host, uint32_t n_seq,
