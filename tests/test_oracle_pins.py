@@ -310,13 +310,14 @@ def pin_placement_and_page_size_invariance():
 
 def pin_split_merge():
     """Any partition of the visible keys, merged by log-sum-exp, equals the
-    unsplit softmax (llama.cpp fork PR #2, LSE commit), over many random
-    splittings, including empty (fully masked) parts."""
+    unsplit softmax (llama.cpp fork PR #2, LSE commit), over 1024 random
+    splittings (the pages' count for their merge oracle), including empty
+    (fully masked) parts."""
     w = W.make_workload("sm", 31, [70, 9], 16, W.TYPE_Q8_0, W.TYPE_Q4_0, 3, "shuffled")
     cache = oracle.Cache.from_workload(w)
     full_out, full_lse = oracle.decode(cache, w.q, w.scale)
     rng = np.random.default_rng(7)
-    for case in range(256):
+    for case in range(1024):
         s = int(rng.integers(0, 2))
         t = int(rng.integers(0, 3))
         h = int(rng.integers(0, HQ))
